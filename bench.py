@@ -1,0 +1,423 @@
+"""Benchmark of the GB300 LoongTrain 2D-Attention ring step.
+
+One step = one pass of the hot path over one batch of synthetic input: the
+Ulysses head-context repack of Q, K and V ((S/P, H) -> (S, H/P) for every ring
+rank's head group), the fused ring-attention forward (online softmax merged
+over the double-ring schedule) and the backward (row statistics, dQ/dK/dV).
+Metric: algorithmic causal TFLOP/s of forward + backward, 7 * B * S^2 * Hq * d
+per step (forward 2 GEMMs over the causal half, backward 2.5x the forward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--no-e2e] [--no-cpu-baseline]
+
+Under torchrun each rank runs the whole workload on its own GPU as an
+independent replica (weak scaling); value = all ranks' FLOPs / max rank time.
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "llama3-8b-s128k"
+METRIC = "causal ring-attention fwd+bwd TFLOP/s and % of GB300 BF16 dense peak"
+SLOWDOWN_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args(argv)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    if n_gpus != world and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE {world}")
+    return rank, local, world, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value, device):
+    """Max of a float over ranks (identity for one rank)."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_inputs(w, x=None):
+    """Head 0 (and its kv head 0) of the workload's seeded inputs as float64
+    numpy arrays [S, 1, d]; drawn on the GPU when one is present."""
+    import torch
+
+    from head_context_attention_gb300 import inputs
+
+    if x is None:
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        x = inputs.make_inputs(w, device=dev, with_do=True)
+    return {n: t[0, :, :1].to("cpu", torch.float64).numpy() for n, t in x.items()}
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_sample(w, seconds, arrays):
+    """Time the float64 oracle on a bounded sample of workload ``w``.
+
+    Sample: query rows of head 0 spread over the sequence; for each row the
+    oracle's forward (softmax over keys 0..i) and backward (dQ row) at the
+    workload's full S.  FLOPs per row i follow the metric's accounting,
+    3.5 * 4 * (i + 1) * d.  Rows are added until ``seconds`` have elapsed.
+    """
+    import numpy as np
+
+    from oracle import attention
+
+    q, k, v, do = arrays["q"], arrays["k"], arrays["v"], arrays["do"]
+    rng = np.random.default_rng(0)
+    rows_done, flops, t0 = 0, 0.0, time.perf_counter()
+    chunk = 8
+    while time.perf_counter() - t0 < seconds:
+        rows = np.sort(rng.integers(0, w.seqlen, size=chunk))
+        attention.attention_rows(q, k, v, rows, [0])
+        attention.attention_backward_rows(q, k, v, do, rows, [0])
+        flops += float(np.sum(3.5 * 4.0 * (rows + 1) * w.head_dim))
+        rows_done += chunk
+    el = time.perf_counter() - t0
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{rows_done} query rows of head 0 at S={w.seqlen} (forward row + dQ row, float64), "
+                      f"{el:.1f} s"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, w, rank, local, world, pg):
+    import torch
+
+    from head_context_attention_gb300 import inputs, ops
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mode = ops.MODE_FUSED if args.mode == "fused" else ops.MODE_STEPWISE
+    desc = ops.make_desc(w, mode)
+    if ops.loong_attn_check(desc) != ops.LOONG_OK:
+        raise SystemExit(f"workload {w.name} rejected: {ops.loong_attn_check(desc)}")
+    x = inputs.make_inputs(w, device=dev, with_do=True)
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws0 = ops.workspace(desc, 0, dev)
+    ws1 = ops.workspace(desc, 1, dev)
+    P = w.hp
+    s_local = w.seqlen // (w.cp * P)
+    packed = {n: torch.empty((w.batch * w.cp, P, w.seqlen // w.cp, t.shape[2] // P, w.head_dim),
+                             dtype=torch.bfloat16, device=dev) for n, t in (("q", q), ("k", k), ("v", v))}
+    stream = torch.cuda.current_stream(dev)
+
+    def repack():
+        for n, t in (("q", q), ("k", k), ("v", v)):
+            ops.loong_headctx_pack(t, packed[n], w.batch, w.cp, P, s_local, t.shape[2], w.head_dim, 0, 1,
+                                   stream)
+
+    def step():
+        repack()
+        ops.loong_attn_fwd(desc, q, k, v, o, lse, ws0, stream)
+        ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
+
+    launches_per_step = 3 + (1 if mode == ops.MODE_FUSED else w.cp + 2) + \
+        (3 if mode == ops.MODE_FUSED else w.cp + 4)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = ops.loong_get_device_status(stream)
+    if st != ops.LOONG_OK:
+        raise SystemExit(f"device status {st} after warm-up")
+
+    # Timed region: K steps; per-kernel events for the forward and backward kernels.
+    ev_f = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev_p[i][0].record(stream)
+            repack()
+            ev_p[i][1].record(stream)
+            ops.loong_set_timing_events(*ev_f[i])
+            ops.loong_attn_fwd(desc, q, k, v, o, lse, ws0, stream)
+            ops.loong_set_timing_events(*ev_b[i])
+            ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
+            ops.loong_set_timing_events(None, None)
+        t_stop.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(pg)
+    st = ops.loong_get_device_status(stream)
+    if st != ops.LOONG_OK:
+        raise SystemExit(f"device status {st} in the timed region")
+    ms_total = t_start.elapsed_time(t_stop)
+    ms_total = max_over_ranks(pg, ms_total, dev)
+    ms_step = ms_total / args.steps
+    f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
+    b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b)
+    p_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_p)
+    peaks = measured_peaks()
+    flops_step = w.flops
+    tflops = flops_step * world / (ms_step * 1e-3) / 1e12
+
+    bwd_flops = w.fwd_flops * 2.5
+    bwd_tf = bwd_flops / (b_ms * 1e-3) / 1e12
+    fwd_tf = w.fwd_flops / (f_ms * 1e-3) / 1e12
+    pack_bytes = 2 * w.batch * w.seqlen * (w.hq + 2 * w.hkv) * w.head_dim * 2
+    pack_gbs = pack_bytes / (p_ms * 1e-3) / 1e9
+    dominant = "bwd" if b_ms >= f_ms else "fwd"
+    dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
+    peak = peaks["bf16_tflops_sustained"]
+    clocks = clk.summary()
+
+    result = {
+        "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, Llama-3-shaped attention layer)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "hq": w.hq, "hkv": w.hkv,
+                   "head_dim": w.head_dim, "hp": w.hp, "cp": w.cp, "ring_inner": w.ring_inner,
+                   "ring_outer": w.ring_outer, "placement": "zigzag" if w.placement == 1 else "contiguous",
+                   "mode": args.mode, "parallelism": f"replicas x{world} (each rank: all hp x cp ranks emulated)",
+                   "l2": "inputs exceed L2 (Q and dO 1 GiB each at this size); no flush",
+                   "flops_per_step": flops_step},
+        "pct_of_peak": round(100.0 * tflops / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": f"ring_{dominant}_kernel", "achieved": round(dom_tf, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(dom_tf / peak, 4),
+                     "peak_kind": f"bf16 sustained, of {peaks['source']}", "traffic": None},
+        "kernels": {
+            "ring_fwd_kernel": {"ms": round(f_ms, 3), "tflops": round(fwd_tf, 2),
+                                "frac_of_peak": round(fwd_tf / peak, 4)},
+            "ring_bwd_kernel": {"ms": round(b_ms, 3), "tflops": round(bwd_tf, 2),
+                                "frac_of_peak": round(bwd_tf / peak, 4)},
+            "headctx_pack_qkv": {"ms": round(p_ms, 3), "gbs": round(pack_gbs, 1),
+                                 "frac_of_hbm": round(pack_gbs / peaks["hbm_gbs"], 4), "bytes": pack_bytes},
+        },
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    rejected = [r for r in clocks.get("reasons", []) if r in SLOWDOWN_REASONS]
+    if rejected:
+        result["clocks"]["rejected"] = rejected
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, w, desc, dev, stream, world, pg, x)
+    return result, x
+
+
+def run_e2e(args, w, desc, dev, stream, world, pg, x):
+    """Same metric through the public API with host buffers: every step copies
+    Q, K, V, dO from pinned host memory and O, LSE, dQ, dK, dV back."""
+    import torch
+
+    from head_context_attention_gb300 import ops
+
+    host_in = {n: t.cpu().pin_memory() for n, t in x.items()}
+    dev_in = {n: torch.empty_like(t) for n, t in x.items()}
+    o = torch.empty_like(dev_in["q"])
+    lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(o), torch.empty_like(dev_in["k"]), torch.empty_like(dev_in["v"])
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    ws0, ws1 = ops.workspace(desc, 0, dev), ops.workspace(desc, 1, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def step():
+        for n in dev_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        ops.loong_attn_fwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, ws0, stream)
+        ops.loong_attn_bwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, dev_in["do"], dq, dk, dv, ws1,
+                           stream)
+        for n in host_out:
+            host_out[n].copy_(outs[n], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(pg)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(pg, a.elapsed_time(b), dev) / args.steps
+    return {"value": round(w.flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from head_context_attention_gb300 import inputs
+
+    if args.workload not in inputs.WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(inputs.WORKLOADS)}")
+    w = inputs.WORKLOADS[args.workload]
+    if not w.backward:
+        w = w.with_(backward=True)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        per_step = max(2.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+        arrays = oracle_inputs(w)
+        for _ in range(args.warmup):
+            cpu_sample(w, per_step, arrays)
+        vals, t0 = [], time.perf_counter()
+        last = None
+        for _ in range(args.steps):
+            last = cpu_sample(w, per_step, arrays)
+            vals.append(last["value"])
+        el = time.perf_counter() - t0
+        v = statistics.mean(vals)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded N(0,1) bf16 widened to float64)",
+                "config": {"workload": w.name, "seqlen": w.seqlen, "hq": w.hq, "hkv": w.hkv,
+                           "head_dim": w.head_dim, "hp": w.hp, "cp": w.cp},
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                                 "sample": last["sample"]},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    rank, local, world, pg = dist_setup(args.gpus)
+    result, x = run_gpu(args, w, rank, local, world, pg)
+    if rank == 0 and not args.no_cpu_baseline:
+        arrays = oracle_inputs(w, x)
+        del x
+        result["cpu_baseline"] = cpu_sample(w, args.cpu_seconds, arrays)
+    if rank == 0:
+        print(json.dumps(result))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

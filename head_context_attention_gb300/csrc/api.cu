@@ -1,0 +1,311 @@
+// api.cu -- the C ABI of include/loong_attn.h: descriptor validation,
+// workspace sizing, the host ring table, tensor-map encoding, the device error
+// word and dispatch to the kernel launchers.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace loong {
+
+namespace {
+
+__device__ unsigned g_error_word;
+
+thread_local char t_last_cuda_error[256] = "no CUDA error";
+thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
+
+struct DeviceCache {
+  std::once_flag once;
+  unsigned* err = nullptr;
+  int cc_major = 0, cc_minor = 0;
+  cudaError_t status = cudaSuccess;
+};
+DeviceCache g_dev[64];
+
+DeviceCache* device_cache() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) return nullptr;
+  DeviceCache* c = &g_dev[dev];
+  std::call_once(c->once, [c, dev]() {
+    void* p = nullptr;
+    cudaError_t e1 = cudaGetSymbolAddress(&p, g_error_word);
+    if (e1 == cudaSuccess) {
+      c->err = static_cast<unsigned*>(p);
+      e1 = cudaMemset(p, 0, sizeof(unsigned));
+    }
+    cudaError_t e2 = cudaDeviceGetAttribute(&c->cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaError_t e3 = cudaDeviceGetAttribute(&c->cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    c->status = e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3);
+  });
+  if (c->status != cudaSuccess) {
+    cuda_fail(c->status);
+    return nullptr;
+  }
+  return c;
+}
+
+bool is_pow2_ok_hd(int d) { return d == 64 || d == 128; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every CUDA-touching entry point checks the device first.
+int device_ready() {
+  DeviceCache* c = device_cache();
+  if (!c) return LOONG_ERR_CUDA;
+  if (!(c->cc_major == 10 && c->cc_minor == 3)) return LOONG_ERR_UNSUPPORTED;
+  return LOONG_OK;
+}
+
+}  // namespace
+
+int cuda_fail(cudaError_t e) {
+  std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return LOONG_ERR_CUDA;
+}
+
+int check_launch() {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LOONG_OK : cuda_fail(e);
+}
+
+void record_start(cudaStream_t s) {
+  if (t_ev_start && t_ev_stop) cudaEventRecord(t_ev_start, s);
+}
+void record_stop(cudaStream_t s) {
+  if (t_ev_start && t_ev_stop) cudaEventRecord(t_ev_stop, s);
+}
+
+unsigned* device_error_word() {
+  DeviceCache* c = device_cache();
+  return c ? c->err : nullptr;
+}
+
+EncodeTiledFn tensor_map_encoder() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int make_head_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return LOONG_ERR_CUDA;
+  if (!aligned16(base)) return LOONG_ERR_INVALID_ARG;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(d) * 2 * static_cast<cuuint64_t>(heads)};
+  const cuuint32_t box[3] = {64, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
+                  static_cast<int>(r));
+    return LOONG_ERR_CUDA;
+  }
+  return LOONG_OK;
+}
+
+RingGeom ring_geom(const loong_attn_desc& d) {
+  RingGeom g;
+  g.cp = d.cp;
+  g.inner = d.ring_inner;
+  g.outer = d.ring_outer;
+  g.zigzag = d.placement == LOONG_PLACEMENT_ZIGZAG;
+  g.nblocks = g.zigzag ? 2 * d.cp : d.cp;
+  g.blk = static_cast<int>(d.seqlen / g.nblocks);
+  g.ntile = (g.blk + kTile - 1) / kTile;
+  return g;
+}
+
+}  // namespace loong
+
+using namespace loong;
+
+extern "C" {
+
+int loong_version(void) { return (0 << 16) | 1; }
+
+const char* loong_status_string(int status) {
+  switch (status) {
+    case LOONG_OK: return "ok";
+    case LOONG_ERR_INVALID_ARG: return "invalid argument";
+    case LOONG_ERR_WORKSPACE: return "workspace too small";
+    case LOONG_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case LOONG_ERR_CUDA: return "CUDA error";
+    case LOONG_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* loong_last_cuda_error(void) { return t_last_cuda_error; }
+
+int loong_attn_check(const loong_attn_desc* d) {
+  if (!d) return LOONG_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->seqlen < 1 || d->hq < 1 || d->hkv < 1 || d->hp < 1 || d->cp < 1 ||
+      d->ring_inner < 1 || d->ring_outer < 1)
+    return LOONG_ERR_INVALID_ARG;
+  if (d->hq % d->hkv || d->hkv % d->hp || d->hq % d->hp) return LOONG_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(d->ring_inner) * d->ring_outer != d->cp) return LOONG_ERR_INVALID_ARG;
+  if (d->placement != LOONG_PLACEMENT_ZIGZAG && d->placement != LOONG_PLACEMENT_CONTIGUOUS)
+    return LOONG_ERR_INVALID_ARG;
+  if (d->mode != LOONG_MODE_FUSED && d->mode != LOONG_MODE_STEPWISE) return LOONG_ERR_INVALID_ARG;
+  const int64_t nblocks = d->placement == LOONG_PLACEMENT_ZIGZAG ? 2 * static_cast<int64_t>(d->cp) : d->cp;
+  if (d->seqlen % nblocks) return LOONG_ERR_INVALID_ARG;
+  if ((d->seqlen / nblocks) % d->hp) return LOONG_ERR_INVALID_ARG;
+  if (d->batch * d->seqlen > 0x7fffffffLL) return LOONG_ERR_UNSUPPORTED;  // TMA row coordinate is int32
+  if (!std::isfinite(d->softmax_scale)) return LOONG_ERR_INVALID_ARG;
+  if (!is_pow2_ok_hd(d->head_dim)) return LOONG_ERR_UNSUPPORTED;
+  if (d->causal != 1) return LOONG_ERR_UNSUPPORTED;
+  return LOONG_OK;
+}
+
+size_t loong_attn_workspace_size(const loong_attn_desc* d, int pass) {
+  if (loong_attn_check(d) != LOONG_OK) return 0;
+  const size_t q_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hq * d->head_dim;
+  const size_t kv_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hkv * d->head_dim;
+  const size_t rows = static_cast<size_t>(d->batch) * d->hq * d->seqlen;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  if (pass == 0) return d->mode == LOONG_MODE_STEPWISE ? up(q_elems * 4) : 0;
+  if (pass != 1) return 0;
+  const size_t stats = 2 * static_cast<size_t>(d->batch) * d->hq * stat_row_len(ring_geom(*d));
+  size_t n = up(q_elems * 4) + up(stats * 4);
+  if (d->mode == LOONG_MODE_STEPWISE) n += 2 * up(kv_elems * 4);
+  return n;
+}
+
+int loong_ring_schedule(int32_t inner, int32_t outer, int32_t* src) {
+  if (!src || inner < 1 || outer < 1 || static_cast<int64_t>(inner) * outer > (1 << 15))
+    return LOONG_ERR_INVALID_ARG;
+  const int cp = inner * outer;
+  for (int t = 0; t < cp; ++t)
+    for (int c = 0; c < cp; ++c) src[static_cast<int64_t>(t) * cp + c] = ring_src(c, t, inner, outer);
+  return LOONG_OK;
+}
+
+int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, void* o,
+                   float* lse, void* ws, size_t ws_bytes, loong_stream_t stream_) {
+  int st = loong_attn_check(d);
+  if (st != LOONG_OK) return st;
+  if (!q || !k || !v || !o || !lse) return LOONG_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return LOONG_ERR_INVALID_ARG;
+  const size_t need = loong_attn_workspace_size(d, 0);
+  if (need && (!ws || ws_bytes < need || !aligned16(ws))) return LOONG_ERR_WORKSPACE;
+  if ((st = device_ready()) != LOONG_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (d->mode == LOONG_MODE_FUSED) return launch_fwd(*d, q, k, v, o, lse, nullptr, stream);
+  const int64_t q_elems = d->batch * d->seqlen * d->hq * d->head_dim;
+  float* o_acc = static_cast<float*>(ws);
+  cudaError_t e = cudaMemsetAsync(o_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((st = launch_fill_f32(lse, d->batch * d->hq * d->seqlen, -INFINITY, stream)) != LOONG_OK) return st;
+  if ((st = launch_fwd(*d, q, k, v, o, lse, o_acc, stream)) != LOONG_OK) return st;
+  return launch_f32_to_bf16(o_acc, o, q_elems, stream);
+}
+
+int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, const void* o,
+                   const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                   size_t ws_bytes, loong_stream_t stream_) {
+  int st = loong_attn_check(d);
+  if (st != LOONG_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return LOONG_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LOONG_ERR_INVALID_ARG;
+  const size_t need = loong_attn_workspace_size(d, 1);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return LOONG_ERR_WORKSPACE;
+  if ((st = device_ready()) != LOONG_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t q_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hq * d->head_dim;
+  const size_t kv_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hkv * d->head_dim;
+  const size_t stats = 2 * static_cast<size_t>(d->batch) * d->hq * stat_row_len(ring_geom(*d));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* dq_acc = reinterpret_cast<float*>(w);
+  float* dvec = reinterpret_cast<float*>(w + up(q_elems * 4));
+  float* dk_acc = nullptr;
+  float* dv_acc = nullptr;
+  if (d->mode == LOONG_MODE_STEPWISE) {
+    dk_acc = reinterpret_cast<float*>(w + up(q_elems * 4) + up(stats * 4));
+    dv_acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dk_acc) + up(kv_elems * 4));
+  }
+  return launch_bwd(*d, q, k, v, o, lse, dout, dq, dk, dv, dq_acc, dvec, dk_acc, dv_acc, stream);
+}
+
+int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts, const float* o_parts, const float* lse_parts,
+                    void* o_out, float* lse_out, int out_bf16, loong_stream_t stream) {
+  if (rows < 0 || d < 1 || d > 1024 || d % 4 || n_parts < 1 || n_parts > 64) return LOONG_ERR_INVALID_ARG;
+  if (out_bf16 != 0 && out_bf16 != 1) return LOONG_ERR_INVALID_ARG;
+  if (rows == 0) return LOONG_OK;
+  if (!o_parts || !lse_parts || !o_out || !lse_out) return LOONG_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(o_out) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+    return LOONG_ERR_INVALID_ARG;
+  int st = device_ready();
+  if (st != LOONG_OK) return st;
+  return launch_lse_merge(rows, d, n_parts, o_parts, lse_parts, o_out, lse_out, out_bf16,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s_local, int32_t heads, int32_t d,
+                       int direction, int gather, const void* in, void* out, loong_stream_t stream) {
+  if (batch < 0 || cp < 1 || P < 1 || s_local < 0 || heads < 1 || d < 1) return LOONG_ERR_INVALID_ARG;
+  if (heads % P || (d * 2) % 16) return LOONG_ERR_INVALID_ARG;
+  if (direction != 0 && direction != 1) return LOONG_ERR_INVALID_ARG;
+  if (gather < 0 || gather > 2) return LOONG_ERR_INVALID_ARG;
+  const int64_t S = static_cast<int64_t>(cp) * P * s_local;
+  if (gather == 1 && (S % (2 * cp))) return LOONG_ERR_INVALID_ARG;
+  if (batch == 0 || s_local == 0) return LOONG_OK;
+  if (!in || !out || !aligned16(in) || !aligned16(out)) return LOONG_ERR_INVALID_ARG;
+  int st = device_ready();
+  if (st != LOONG_OK) return st;
+  return launch_headctx_pack(batch, cp, P, s_local, heads, d, direction, gather, in, out,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int loong_set_timing_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return LOONG_ERR_INVALID_ARG;
+  t_ev_start = static_cast<cudaEvent_t>(start_event);
+  t_ev_stop = static_cast<cudaEvent_t>(stop_event);
+  return LOONG_OK;
+}
+
+int loong_get_device_status(loong_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned* p = device_error_word();
+  if (!p) return LOONG_ERR_CUDA;
+  unsigned word = 0;
+  e = cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word) {
+    e = cudaMemset(p, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return LOONG_ERR_DEVICE_TIMEOUT;
+  }
+  return LOONG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,565 @@
+// attn_bwd.cu -- backward ring-step attention on tcgen05 tensor cores.
+//
+// The gradient of causal softmax attention (plain chain rule; the pages give no
+// backward).  One CTA owns one 128-key tile of one kv head and walks every
+// (query tile, query head of the group) that attends to it, in the order the
+// key/value chunk travels around the ring: step t visits ring rank
+// dst(j, t), the rank that holds source j's K/V at step t.  Per iteration:
+//   S^T  = K Q^T                 (keys on TMEM lanes, queries on columns)
+//   dP^T = V dO^T
+//   P^T  = exp2(S^T*scale*log2e - LSE*log2e),  dS^T = P^T * (dP^T - D)
+//   dV  += P^T dO                (P^T from tensor memory)
+//   dK  += dS^T Q                (dS^T from shared memory, K-major)
+//   dQ   = dS K  -> fp32 atomics into the dQ accumulator (dS^T read MN-major)
+// dK and dV stay in tensor memory for the whole walk and are written once
+// (FUSED) or added into fp32 accumulators (STEPWISE, one launch per step; a
+// step maps ranks to sources one to one, so no two CTAs share a tile).
+//
+// Warp roles (320 threads): warps 0-3 and 4-7 form two groups that each cover
+// all 128 TMEM lanes; group w handles query columns [64w, 64w+64) of S^T/dP^T
+// and head-dim columns [D/2*w, D/2*(w+1)) of dQ; warp 8 issues TMA loads,
+// warp 9 allocates TMEM and issues the MMAs.
+// Tensor memory (512 columns): R0 [0,128) S^T then P^T (bf16 pairs, first 64
+// columns); R1 [128,256) dP^T then dQ; dV and dK after that (D columns each).
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace loong {
+
+namespace {
+
+template <int D>
+struct BwdCfg {
+  static constexpr int NS = 2;                    // Q / dO pipeline stages
+  static constexpr int ATOMS = D / 64;
+  static constexpr int ATOM_BYTES = kTile * 128;  // 16 KB
+  static constexpr int TILE_BYTES = kTile * D * 2;
+  static constexpr int DS_BYTES = kTile * kTile * 2;  // dS^T tile, bf16 [keys][queries]
+  static constexpr int NBARS = 1 + 2 * NS + 6;
+  static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NBARS * 8 + 1024;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t R0 = 0, R1 = 128, RV = 256, RK = 256 + D;
+};
+
+struct BwdArgs {
+  int batch, S, hq, hkv, G;
+  RingGeom ring;
+  int t_begin, t_end;
+  float scale, scale_log2;
+  // Row statistics, [B*Hq][stat_len] each, block b's rows at b*blk_pad:
+  const float* lse2;   // LSE * log2(e)
+  const float* dstat;  // D = rowsum(dO * O)
+  int blk_pad, stat_len;
+  float* dq_acc;      // [B, S, Hq, D] fp32
+  __nv_bfloat16* dk;  // FUSED outputs
+  __nv_bfloat16* dv;
+  float* dk_acc;      // STEPWISE accumulators
+  float* dv_acc;
+  unsigned* err;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__host__ __device__ inline int ring_dst(int j, int t, int inner, int outer) {
+  const int o = t / inner, i = t - (t / inner) * inner;
+  const int g = j / inner, l = j - (j / inner) * inner;
+  return ((g + o) % outer) * inner + (l + i) % inner;
+}
+
+// The (query tile, head) pairs that meet key tile (block bk, tile kt) over
+// ring steps [t0, t1), in the order the K/V chunk visits ranks.
+struct QWalk {
+  RingGeom g;
+  int G, bk, kt, j, t, t1, part, qi, qi_end, head, bq;
+
+  __device__ void init(const RingGeom& geom, int G_, int bk_, int kt_, int t0, int t1_) {
+    g = geom;
+    G = G_;
+    bk = bk_;
+    kt = kt_;
+    j = block_owner(g, bk);
+    t = t0;
+    t1 = t1_;
+    part = 0;
+    qi = -1;
+    head = 0;
+    next_block();
+  }
+  // Position on the first query tile of the next block that sees bk.
+  __device__ void next_block() {
+    while (t < t1) {
+      if (qi < 0) {
+        const int c = ring_dst(j, t, g.inner, g.outer);
+        bq = rank_block(g, c, part);
+        qi_end = g.ntile;
+        qi = bk < bq ? 0 : (bk == bq ? kt : g.ntile);
+        if (qi < qi_end) return;
+      }
+      qi = -1;
+      if (++part == rank_parts(g)) {
+        part = 0;
+        ++t;
+      }
+    }
+  }
+  __device__ bool done() const { return t >= t1; }
+  __device__ void advance() {
+    if (++head < G) return;
+    head = 0;
+    if (++qi < qi_end) return;
+    qi = -1;
+    if (++part == rank_parts(g)) {
+      part = 0;
+      ++t;
+    }
+    next_block();
+  }
+  __device__ int q0() const { return bq * g.blk + qi * kTile; }
+  __device__ int qlen() const {
+    const int e = (bq + 1) * g.blk - q0();
+    return e < kTile ? e : kTile;
+  }
+  __device__ bool diag() const { return bq == bk && qi == kt; }
+  __device__ int count() const {
+    int n = 0;
+    for (int tt = t; tt < t1; ++tt) {
+      const int c = ring_dst(j, tt, g.inner, g.outer);
+      for (int pp = 0; pp < rank_parts(g); ++pp) {
+        const int b = rank_block(g, c, pp);
+        if (bk < b) n += g.ntile;
+        else if (bk == b) n += g.ntile - kt;
+      }
+    }
+    return n * G;
+  }
+};
+
+template <int D, bool STEP>
+__global__ void __launch_bounds__(320, 1)
+    ring_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = sK + C::TILE_BYTES;
+  uint8_t* sQ = sV + C::TILE_BYTES;              // NS stages
+  uint8_t* sdO = sQ + C::NS * C::TILE_BYTES;     // NS stages
+  uint8_t* sdS = sdO + C::NS * C::TILE_BYTES;    // [2 query atoms][128 keys][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sdS + C::DS_BYTES);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + C::NS;
+  uint64_t* sd_full = q_empty + C::NS;
+  uint64_t* pd_full = sd_full + 1;
+  uint64_t* dq_full = pd_full + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* done_bar = dq_empty + 1;
+  uint64_t* drain = done_bar + 1;
+  volatile int* abort_flag = &abort_sh;
+
+  // ---- work item: (batch, kv head, key tile); early (heavy) key tiles first
+  const RingGeom& g = a.ring;
+  int idx = blockIdx.x;
+  const int nkt = g.nblocks * g.ntile;
+  const int r = idx % nkt;
+  idx /= nkt;
+  const int kvh = idx % a.hkv;
+  const int b = idx / a.hkv;
+  const int bk = r / g.ntile;
+  const int kt = r % g.ntile;
+  const int k0 = bk * g.blk + kt * kTile;
+  const int klen = min(kTile, (bk + 1) * g.blk - k0);
+
+  QWalk walk;
+  walk.init(g, a.G, bk, kt, a.t_begin, a.t_end);
+  const int n = walk.count();
+  if (n == 0) return;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    mbar_init(sd_full, 1);
+    mbar_init(pd_full, 8);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 8);
+    mbar_init(done_bar, 1);
+    mbar_init(drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+    tma_prefetch_map(&tmO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_sh;
+  const int64_t row_base = static_cast<int64_t>(b) * a.S;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(kv_full, 2 * C::TILE_BYTES);
+      for (int at = 0; at < C::ATOMS; ++at) {
+        tma_load_3d(sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvh, static_cast<int>(row_base + k0));
+        tma_load_3d(sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvh, static_cast<int>(row_base + k0));
+      }
+      int issued = 0;
+      for (int i = 0; i < n; ++i, walk.advance()) {
+        const int s = i % C::NS;
+        const int u = i / C::NS;
+        if (i >= C::NS && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
+        const int head = kvh * a.G + walk.head;
+        const int qrow = static_cast<int>(row_base + walk.q0());
+        mbar_expect_tx(&q_full[s], 2 * C::TILE_BYTES);
+        for (int at = 0; at < C::ATOMS; ++at) {
+          tma_load_3d(sQ + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, &q_full[s], at * 64, head, qrow);
+          tma_load_3d(sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, head, qrow);
+        }
+        ++issued;
+      }
+      mbar_drain(kv_full, 0, a.err);
+      for (int s = 0; s < C::NS; ++s) {
+        const int cnt = issued > s ? (issued - 1 - s) / C::NS + 1 : 0;
+        if (cnt) mbar_drain(&q_full[s], (cnt - 1) & 1, a.err);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
+      constexpr uint32_t id_dkv = idesc_bf16(128, D, false, true);   // dV, dK: B MN-major
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // dQ: A and B MN-major
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
+                     o_addr = smem_u32(sdO), ds_addr = smem_u32(sdS);
+      // X^T[keys x queries] = A[keys x d] * B[queries x d]^T, both K-major
+      auto mm_s = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
+          mma_ss(tbase + dst, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), id_s,
+                 kk > 0);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, a.err) && mbar_wait(&q_full[0], 0, abort_flag, a.err);
+      if (ok) {
+        tc_fence_after();
+        mm_s(C::R0, k_addr, q_addr);
+        mm_s(C::R1, v_addr, o_addr);
+        mma_commit(sd_full);
+        for (int i = 0; i < n; ++i) {
+          const int s = i % C::NS;
+          if (!mbar_wait(pd_full, i & 1, abort_flag, a.err)) break;
+          tc_fence_after();
+          const uint32_t qs = q_addr + s * C::TILE_BYTES, os = o_addr + s * C::TILE_BYTES;
+          // dV += P^T dO: A = P^T (TMEM, 8 columns per 16 queries), B = dO MN-major
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ts(tbase + C::RV, tbase + C::R0 + kk * 8, sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv,
+                   i > 0 || kk > 0);
+          // dK += dS^T Q: A = dS^T K-major (queries contiguous), B = Q MN-major
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
+            mma_ss(tbase + C::RK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::ATOM_BYTES, 1024),
+                   id_dkv, i > 0 || kk > 0);
+          }
+          // dQ = dS K: A = dS (dS^T read MN-major), B = K MN-major
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tbase + C::R1, sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024),
+                   sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024), id_dq, kk > 0);
+          mma_commit(dq_full);
+          mma_commit(&q_empty[s]);
+          if (i + 1 < n) {
+            const int s1 = (i + 1) % C::NS;
+            if (!mbar_wait(&q_full[s1], ((i + 1) / C::NS) & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+            mm_s(C::R0, k_addr, q_addr + s1 * C::TILE_BYTES);
+            if (!mbar_wait(dq_empty, i & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+            mm_s(C::R1, v_addr, o_addr + s1 * C::TILE_BYTES);
+            mma_commit(sd_full);
+          }
+        }
+        mma_commit(done_bar);
+      }
+      mma_commit(drain);
+      mbar_drain(drain, 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int grp = warp >> 2;  // query columns [64 grp, 64 grp + 64)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // key row in the pass, query row in the dQ drain
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool key_ok = row < klen;
+    bool ok = true;
+    for (int i = 0; i < n; ++i, walk.advance()) {
+      if (!__all_sync(0xffffffffu, mbar_wait(sd_full, i & 1, abort_flag, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int head = kvh * a.G + walk.head;
+      const int q0 = walk.q0();
+      const int qlen = walk.qlen();
+      const bool dg = walk.diag();
+      const float* lse_row = a.lse2 + (static_cast<int64_t>(b) * a.hq + head) * a.stat_len;
+      const float* d_row = a.dstat + (static_cast<int64_t>(b) * a.hq + head) * a.stat_len;
+      const int qidx = walk.bq * a.blk_pad + walk.qi * kTile;
+      // Two 32-column chunks of this group's 64 queries.
+#pragma unroll 1
+      for (int ch = 0; ch < 2; ++ch) {
+        const int cbase = grp * 64 + ch * 32;  // first query column of the chunk
+        uint32_t sv[32], dpv[32];
+        tmem_ld32(tbase + t_lane + C::R0 + cbase, sv);
+        tmem_ld32(tbase + t_lane + C::R1 + cbase, dpv);
+        tmem_wait_ld();
+        uint32_t pk[16];
+        uint32_t dsk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          // the same query indices in every lane: broadcast loads of the
+          // padded per-block row statistics (aligned, always in bounds)
+          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_row + qidx + cbase + e));
+          const float4 d4 = __ldg(reinterpret_cast<const float4*>(d_row + qidx + cbase + e));
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = cbase + e + u;
+            const bool live = key_ok && c < qlen && (!dg || row <= c);
+            // masked columns may hold statistics of other rows or padding: select, never multiply
+            const float x = fast_exp2(fmaf(__uint_as_float(sv[e + u]), a.scale_log2, -lv[u]));
+            p[u] = live ? x : 0.f;
+            ds[u] = live ? x * (__uint_as_float(dpv[e + u]) - dv4[u]) : 0.f;
+          }
+          pk[e / 2] = pack_bf16(p[0], p[1]);
+          pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
+          dsk[e / 2] = pack_bf16(ds[0], ds[1]);
+          dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+        }
+        // P^T (bf16 pairs) into R0 columns [cbase/2, cbase/2 + 16)
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tbase + t_lane + C::R0 + cbase / 2),
+            "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]),
+            "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
+            : "memory");
+        // dS^T row `row`, queries [cbase, cbase+32): 4 of the 8 16-byte units of
+        // this group's 128-byte line in atom `grp`, 128-byte swizzled.
+        uint8_t* line = sdS + grp * C::ATOM_BYTES + row * 128;
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int unit = ch * 4 + uu;
+          uint4 w;
+          w.x = dsk[uu * 4 + 0];
+          w.y = dsk[uu * 4 + 1];
+          w.z = dsk[uu * 4 + 2];
+          w.w = dsk[uu * 4 + 3];
+          *reinterpret_cast<uint4*>(line + ((unit ^ (row & 7)) << 4)) = w;
+        }
+      }
+      tmem_wait_st();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pd_full);
+
+      // ---- drain dQ (queries on lanes) into the fp32 accumulator
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, i & 1, abort_flag, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const bool q_ok = row < qlen;
+        float* dst = a.dq_acc + ((row_base + q0 + row) * a.hq + head) * D + grp * (D / 2);
+#pragma unroll 1
+        for (int cb = 0; cb < D / 64; ++cb) {
+          uint32_t qv[32];
+          tmem_ld32(tbase + t_lane + C::R1 + grp * (D / 2) + cb * 32, qv);
+          tmem_wait_ld();
+          if (q_ok) {
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 x = make_float4(__uint_as_float(qv[v4 * 4]) * a.scale, __uint_as_float(qv[v4 * 4 + 1]) * a.scale,
+                                     __uint_as_float(qv[v4 * 4 + 2]) * a.scale,
+                                     __uint_as_float(qv[v4 * 4 + 3]) * a.scale);
+              atomicAdd(reinterpret_cast<float4*>(dst + cb * 32) + v4, x);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, a.err));
+    if (ok) {
+      tc_fence_after();
+      // group 0 writes dV, group 1 writes dK (keys on lanes)
+      const uint32_t src = grp == 0 ? C::RV : C::RK;
+      const float mul = grp == 0 ? 1.f : a.scale;
+      const int64_t krow = (row_base + k0 + row) * a.hkv + kvh;
+#pragma unroll 1
+      for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t v[32];
+        tmem_ld32(tbase + t_lane + src + cb * 32, v);
+        tmem_wait_ld();
+        if (key_ok) {
+          if constexpr (!STEP) {
+            __nv_bfloat16* dst = (grp == 0 ? a.dv : a.dk) + krow * D + cb * 32;
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(v[v4 * 8 + 0]) * mul, __uint_as_float(v[v4 * 8 + 1]) * mul);
+              w.y = pack_bf16(__uint_as_float(v[v4 * 8 + 2]) * mul, __uint_as_float(v[v4 * 8 + 3]) * mul);
+              w.z = pack_bf16(__uint_as_float(v[v4 * 8 + 4]) * mul, __uint_as_float(v[v4 * 8 + 5]) * mul);
+              w.w = pack_bf16(__uint_as_float(v[v4 * 8 + 6]) * mul, __uint_as_float(v[v4 * 8 + 7]) * mul);
+              reinterpret_cast<uint4*>(dst)[v4] = w;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>((grp == 0 ? a.dv_acc : a.dk_acc) + krow * D + cb * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 x = dst[v4];
+              x.x += __uint_as_float(v[v4 * 4 + 0]) * mul;
+              x.y += __uint_as_float(v[v4 * 4 + 1]) * mul;
+              x.z += __uint_as_float(v[v4 * 4 + 2]) * mul;
+              x.w += __uint_as_float(v[v4 * 4 + 3]) * mul;
+              dst[v4] = x;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool STEP>
+int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const void* v, const void* dout,
+                 const float* stats, float* dq_acc, void* dk, void* dv, float* dk_acc,
+                 float* dv_acc, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int64_t rows = d.batch * d.seqlen;
+  CUtensorMap mq, mk, mv, mo;
+  int st;
+  if ((st = make_head_tile_map(&mq, q, rows, d.hq, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mk, k, rows, d.hkv, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mv, v, rows, d.hkv, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mo, dout, rows, d.hq, D)) != LOONG_OK) return st;
+  BwdArgs a;
+  a.batch = static_cast<int>(d.batch);
+  a.S = static_cast<int>(d.seqlen);
+  a.hq = d.hq;
+  a.hkv = d.hkv;
+  a.G = d.hq / d.hkv;
+  a.ring = ring_geom(d);
+  a.scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  a.scale_log2 = a.scale * kLog2e;
+  a.lse2 = stats;
+  a.blk_pad = stat_block_pad(a.ring.blk);
+  a.stat_len = static_cast<int>(stat_row_len(a.ring));
+  a.dstat = stats + d.batch * d.hq * static_cast<int64_t>(a.stat_len);
+  a.dq_acc = dq_acc;
+  a.dk = static_cast<__nv_bfloat16*>(dk);
+  a.dv = static_cast<__nv_bfloat16*>(dv);
+  a.dk_acc = dk_acc;
+  a.dv_acc = dv_acc;
+  a.err = device_error_word();
+  if (!a.err) return LOONG_ERR_CUDA;
+  auto kern = ring_bwd_kernel<D, STEP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int64_t grid = d.batch * d.hkv * static_cast<int64_t>(a.ring.nblocks) * a.ring.ntile;
+  if (grid <= 0 || grid > 0x7fffffff) return LOONG_ERR_INVALID_ARG;
+  const int t_first = 0, t_last = d.cp;
+  if (!STEP) {
+    a.t_begin = t_first;
+    a.t_end = t_last;
+    record_start(stream);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, a);
+    record_stop(stream);
+    return check_launch();
+  }
+  record_start(stream);
+  for (int t = t_first; t < t_last; ++t) {
+    a.t_begin = t;
+    a.t_end = t + 1;
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, a);
+    if ((st = check_launch()) != LOONG_OK) return st;
+  }
+  record_stop(stream);
+  return LOONG_OK;
+}
+
+}  // namespace
+
+int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, const void* o,
+               const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dq_acc, float* dvec,
+               float* dk_acc, float* dv_acc, cudaStream_t stream) {
+  const int64_t q_elems = d.batch * d.seqlen * d.hq * d.head_dim;
+  const int64_t kv_elems = d.batch * d.seqlen * d.hkv * d.head_dim;
+  const bool step = d.mode == LOONG_MODE_STEPWISE;
+  int st;
+  cudaError_t e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (step) {
+    if ((e = cudaMemsetAsync(dk_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(dv_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if ((st = launch_bwd_rowstats(d, o, dout, lse, dvec, stream)) != LOONG_OK) return st;
+  if (d.head_dim == 128)
+    st = step ? launch_bwd_t<128, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream)
+              : launch_bwd_t<128, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream);
+  else if (d.head_dim == 64)
+    st = step ? launch_bwd_t<64, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream)
+              : launch_bwd_t<64, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream);
+  else
+    return LOONG_ERR_UNSUPPORTED;
+  if (st != LOONG_OK) return st;
+  if ((st = launch_f32_to_bf16(dq_acc, dq, q_elems, stream)) != LOONG_OK) return st;
+  if (step) {
+    if ((st = launch_f32_to_bf16(dk_acc, dk, kv_elems, stream)) != LOONG_OK) return st;
+    if ((st = launch_f32_to_bf16(dv_acc, dv, kv_elems, stream)) != LOONG_OK) return st;
+  }
+  return LOONG_OK;
+}
+
+}  // namespace loong

@@ -1,0 +1,472 @@
+// attn_fwd.cu -- forward ring-step attention on tcgen05 tensor cores.
+//
+// One CTA owns one 128-token query tile of two query heads that share a kv
+// head, and walks the key tiles that tile meets along its ring pass (ring.cuh)
+// in ring order.  Per key tile j and query head h:
+//   S_h = Q_h K_j^T                 tcgen05.mma, operands in shared memory
+//   P_h = exp2(S_h*scale*log2e - m) softmax warps, one thread per query row
+//   O_h += P_h V_j                  tcgen05.mma, P from tensor memory
+// with a running row maximum m and row sum l.  The per-step "merge" of
+// [G] "Guide to LoongTrain", "Step 3" (partial results of successive ring
+// steps) is the online-softmax update itself: O and l carry the reference
+// maximum m, and a step whose maximum exceeds m by more than 2^8 rescales O
+// and l to the new maximum, which is the log-sum-exp merge written in
+// unnormalised form.  In STEPWISE mode the launch covers one ring step and the
+// epilogue merges the step's normalised result into an fp32 accumulator by
+// log-sum-exp.
+//
+// Warp roles (320 threads): warps 0-3 softmax for head slot 0, warps 4-7 for
+// head slot 1 (warp w reads TMEM lanes 32*(w%4)..+31, the rows it owns),
+// warp 8 issues TMA loads, warp 9 allocates TMEM and issues the MMAs.
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
+// that (d columns each).  P_h overwrites the first 64 columns of S_h as bf16
+// pairs; the next Q K^T into S_h is issued after O_h += P_h V and tcgen05
+// operations issued by one thread execute in order.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace loong {
+
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NQ = 2;                     // query tiles (heads) per CTA
+  static constexpr int NS = D == 128 ? 2 : 4;      // K and V pipeline stages
+  static constexpr int ATOMS = D / 64;             // 128-byte swizzle atoms per row
+  static constexpr int ATOM_BYTES = kTile * 128;   // one atom column of a tile
+  static constexpr int TILE_BYTES = kTile * D * 2;
+  static constexpr int NBARS = 1 + 4 * NS + 2 + 2 + 2;
+  static constexpr int SMEM_BYTES = (NQ + 2 * NS) * TILE_BYTES + NBARS * 8 + 1024;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t S_COL(int h) { return static_cast<uint32_t>(h) * 128u; }
+  static constexpr uint32_t O_COL(int h) { return 256u + static_cast<uint32_t>(h) * D; }
+};
+
+struct FwdArgs {
+  int batch, S, hq, hkv, G, npairs;
+  RingGeom ring;
+  int t_begin, t_end;
+  float scale_log2;
+  __nv_bfloat16* o;
+  float* lse;
+  float* o_acc;  // STEPWISE accumulator, else null
+  unsigned* err;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D, bool STEP>
+__global__ void __launch_bounds__(320, 1)
+    ring_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + C::NQ * C::TILE_BYTES;
+  uint8_t* sV = sK + C::NS * C::TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + C::NS * C::TILE_BYTES);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + C::NS;
+  uint64_t* v_full = k_empty + C::NS;
+  uint64_t* v_empty = v_full + C::NS;
+  uint64_t* s_full = v_empty + C::NS;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_final = p_full + 2;
+  uint64_t* drain = o_final + 1;
+  volatile int* abort_flag = &abort_sh;
+
+  // ---- work item: (batch, kv head, query tile, head pair); heavy tiles first
+  const RingGeom& g = a.ring;
+  int idx = blockIdx.x;
+  const int hpair = idx % a.npairs;
+  idx /= a.npairs;
+  const int nqt = g.nblocks * g.ntile;
+  const int r = idx % nqt;
+  idx /= nqt;
+  const int kvh = idx % a.hkv;
+  const int b = idx / a.hkv;
+  const int bq = g.nblocks - 1 - r / g.ntile;
+  const int qi = g.ntile - 1 - r % g.ntile;
+  const int q0 = bq * g.blk + qi * kTile;
+  const int qlen = min(kTile, (bq + 1) * g.blk - q0);
+  const int head0 = kvh * a.G + 2 * hpair;
+  const bool dup = head0 + 1 >= (kvh + 1) * a.G;  // odd group: slot 1 repeats slot 0
+  const int head1 = dup ? head0 : head0 + 1;
+
+  KvWalk walk;
+  walk.init(g, bq, qi, a.t_begin, a.t_end);
+  const int n = walk.count();
+  if (n == 0) return;  // uniform over the CTA: nothing of this tile in these steps
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], 4);
+    }
+    mbar_init(o_final, 1);
+    mbar_init(drain, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_sh;
+  const int64_t row_base = static_cast<int64_t>(b) * a.S;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      mbar_expect_tx(q_full, C::NQ * C::TILE_BYTES);
+      for (int h = 0; h < C::NQ; ++h)
+        for (int at = 0; at < C::ATOMS; ++at)
+          tma_load_3d(sQ + h * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, q_full, at * 64,
+                      h ? head1 : head0, static_cast<int>(row_base + q0));
+      int jk = 0, jv = 0;
+      for (int j = 0; j < n; ++j, walk.advance()) {
+        const int s = j % C::NS;
+        const int u = j / C::NS;
+        const int k0 = static_cast<int>(row_base + walk.k0());
+        if (j >= C::NS && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
+        mbar_expect_tx(&k_full[s], C::TILE_BYTES);
+        for (int at = 0; at < C::ATOMS; ++at)
+          tma_load_3d(sK + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmK, &k_full[s], at * 64, kvh,
+                      k0);
+        ++jk;
+        if (j >= C::NS && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
+        mbar_expect_tx(&v_full[s], C::TILE_BYTES);
+        for (int at = 0; at < C::ATOMS; ++at)
+          tma_load_3d(sV + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmV, &v_full[s], at * 64, kvh,
+                      k0);
+        ++jv;
+      }
+      // Let every copy this thread issued land before the CTA can exit.
+      mbar_drain(q_full, 0, a.err);
+      for (int s = 0; s < C::NS; ++s) {
+        const int nk = jk > s ? (jk - 1 - s) / C::NS + 1 : 0;
+        const int nv = jv > s ? (jv - 1 - s) / C::NS + 1 : 0;
+        if (nk) mbar_drain(&k_full[s], (nk - 1) & 1, a.err);
+        if (nv) mbar_drain(&v_full[s], (nv - 1) & 1, a.err);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
+      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      auto qk = [&](int h, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
+          const uint64_t da = sdesc_sw128(q_addr + h * C::TILE_BYTES + off, 16, 1024);
+          const uint64_t db = sdesc_sw128(k_addr + s * C::TILE_BYTES + off, 16, 1024);
+          mma_ss(tbase + C::S_COL(h), da, db, id_qk, kk > 0);
+        }
+      };
+      auto pv = [&](int h, int s, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t db = sdesc_sw128(v_addr + s * C::TILE_BYTES + kk * 2048, C::ATOM_BYTES, 1024);
+          mma_ts(tbase + C::O_COL(h), tbase + C::S_COL(h) + kk * 8, db, id_pv, acc || kk > 0);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, a.err) &&
+                mbar_wait(&k_full[0], 0, abort_flag, a.err);
+      if (ok) {
+        tc_fence_after();
+        qk(0, 0);
+        mma_commit(&s_full[0]);
+        qk(1, 0);
+        mma_commit(&s_full[1]);
+        mma_commit(&k_empty[0]);
+        for (int j = 0; j < n && ok; ++j) {
+          const int s = j % C::NS;
+          const bool more = j + 1 < n;
+          const int s1 = (j + 1) % C::NS;
+          if (!mbar_wait(&v_full[s], (j / C::NS) & 1, abort_flag, a.err)) break;
+          if (!mbar_wait(&p_full[0], j & 1, abort_flag, a.err)) break;
+          tc_fence_after();
+          pv(0, s, j > 0);
+          if (more) {
+            if (!mbar_wait(&k_full[s1], ((j + 1) / C::NS) & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+            qk(0, s1);
+            mma_commit(&s_full[0]);
+          }
+          if (!mbar_wait(&p_full[1], j & 1, abort_flag, a.err)) break;
+          tc_fence_after();
+          pv(1, s, j > 0);
+          mma_commit(&v_empty[s]);
+          if (more) {
+            qk(1, s1);
+            mma_commit(&s_full[1]);
+            mma_commit(&k_empty[s1]);
+          }
+        }
+        mma_commit(o_final);
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      mma_commit(drain);
+      mbar_drain(drain, 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int h = warp >> 2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tbase + t_lane + C::S_COL(h);
+    const uint32_t tO = tbase + t_lane + C::O_COL(h);
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j, walk.advance()) {
+      // Lanes leave together so the .sync.aligned TMEM accesses never diverge.
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[h], j & 1, abort_flag, a.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tmem_ld32(tS + cb * 32, sr[cb]);
+      tmem_wait_ld();
+      const int klen = walk.klen();
+      const bool dg = walk.diag();
+      if (dg || klen < kTile) {
+        const int lim = dg ? min(row, klen - 1) : klen - 1;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (cb * 32 + i > lim) sr[cb][i] = __float_as_uint(-INFINITY);
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[cb][i]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[cb][i + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[cb][i + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[cb][i + 3]));
+        }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = fmaxf(m_run, m_tile);
+      if (j == 0) {
+        m_run = m_new;
+      } else if (m_new > m_run + kRescaleThreshold) {
+        // O_h is stable: the commit that signalled S_h follows O_h += P V.
+        const float f = fast_exp2(m_run - m_new);
+        l_run *= f;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t orow[32];
+          tmem_ld32(tO + cb * 32, orow);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
+          tmem_st32(tO + cb * 32, orow);
+        }
+        m_run = m_new;
+      }
+      const float ref = m_run == -INFINITY ? 0.f : m_run;
+      float l0 = 0.f, l1 = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[cb][i]), sl2, -ref));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[cb][i + 1]), sl2, -ref));
+          l0 += p0;
+          l1 += p1;
+          pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
+        }
+      l_run += l0 + l1;
+      tmem_st32(tS, pk[0]);
+      tmem_st32(tS + 32, pk[1]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[h]);
+    }
+    // ---------------------------------------------------------- epilogue
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, abort_flag, a.err));
+    if (ok) {
+      tc_fence_after();
+      const int head = h ? head1 : head0;
+      const bool valid = row < qlen && !(h == 1 && dup);
+      const int64_t q = row_base + q0 + row;
+      const float lse_p = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      float* lse_ptr = a.lse + (static_cast<int64_t>(b) * a.hq + head) * a.S + (q0 + row);
+      if constexpr (!STEP) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16* orow = a.o + (q * a.hq + head) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t ov[32];
+          tmem_ld32(tO + cb * 32, ov);
+          tmem_wait_ld();
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(ov[v4 * 8 + 0]) * inv, __uint_as_float(ov[v4 * 8 + 1]) * inv);
+              w.y = pack_bf16(__uint_as_float(ov[v4 * 8 + 2]) * inv, __uint_as_float(ov[v4 * 8 + 3]) * inv);
+              w.z = pack_bf16(__uint_as_float(ov[v4 * 8 + 4]) * inv, __uint_as_float(ov[v4 * 8 + 5]) * inv);
+              w.w = pack_bf16(__uint_as_float(ov[v4 * 8 + 6]) * inv, __uint_as_float(ov[v4 * 8 + 7]) * inv);
+              dst[v4] = w;
+            }
+          }
+        }
+        if (valid) *lse_ptr = lse_p;
+      } else {
+        // Log-sum-exp merge of this step's (O_p, L_p) into (O_acc, L_acc).
+        float ca = 0.f, cpart = 0.f, lse_new = -INFINITY;
+        if (valid) {
+          const float la = *lse_ptr;
+          const float mm = fmaxf(la, lse_p);
+          const float wa = la == -INFINITY ? 0.f : exp2f((la - mm) * kLog2e);
+          const float wp = lse_p == -INFINITY ? 0.f : exp2f((lse_p - mm) * kLog2e);
+          const float tot = wa + wp;
+          if (tot > 0.f) {
+            ca = wa / tot;
+            cpart = wp / (tot * l_run);
+            lse_new = mm + log2f(tot) * kLn2;
+          }
+        }
+        float* acc = a.o_acc + (q * a.hq + head) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t ov[32];
+          tmem_ld32(tO + cb * 32, ov);
+          tmem_wait_ld();
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(acc + cb * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 x = dst[v4];
+              x.x = ca * x.x + cpart * __uint_as_float(ov[v4 * 4 + 0]);
+              x.y = ca * x.y + cpart * __uint_as_float(ov[v4 * 4 + 1]);
+              x.z = ca * x.z + cpart * __uint_as_float(ov[v4 * 4 + 2]);
+              x.w = ca * x.w + cpart * __uint_as_float(ov[v4 * 4 + 3]);
+              dst[v4] = x;
+            }
+          }
+        }
+        if (valid) *lse_ptr = lse_new;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool STEP>
+int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
+                 float* lse, float* o_acc, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  const int64_t rows = d.batch * d.seqlen;
+  CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = make_head_tile_map(&mq, q, rows, d.hq, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mk, k, rows, d.hkv, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mv, v, rows, d.hkv, D)) != LOONG_OK) return st;
+
+  FwdArgs a;
+  a.batch = static_cast<int>(d.batch);
+  a.S = static_cast<int>(d.seqlen);
+  a.hq = d.hq;
+  a.hkv = d.hkv;
+  a.G = d.hq / d.hkv;
+  a.npairs = (a.G + 1) / 2;
+  a.ring = ring_geom(d);
+  const float scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  a.scale_log2 = scale * kLog2e;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.o_acc = o_acc;
+  a.err = device_error_word();
+  if (!a.err) return LOONG_ERR_CUDA;
+
+  auto kern = ring_fwd_kernel<D, STEP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int64_t grid = d.batch * d.hkv * static_cast<int64_t>(a.ring.nblocks) * a.ring.ntile * a.npairs;
+  if (grid <= 0 || grid > 0x7fffffff) return LOONG_ERR_INVALID_ARG;
+  if (!STEP) {
+    a.t_begin = 0;
+    a.t_end = d.cp;
+    record_start(stream);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+    record_stop(stream);
+    return check_launch();
+  }
+  record_start(stream);
+  for (int t = 0; t < d.cp; ++t) {
+    a.t_begin = t;
+    a.t_end = t + 1;
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, a);
+    if ((st = check_launch()) != LOONG_OK) return st;
+  }
+  record_stop(stream);
+  return LOONG_OK;
+}
+
+}  // namespace
+
+int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
+               float* lse, float* o_acc, cudaStream_t stream) {
+  const bool step = d.mode == LOONG_MODE_STEPWISE;
+  if (d.head_dim == 128)
+    return step ? launch_fwd_t<128, true>(d, q, k, v, o, lse, o_acc, stream)
+                : launch_fwd_t<128, false>(d, q, k, v, o, lse, o_acc, stream);
+  if (d.head_dim == 64)
+    return step ? launch_fwd_t<64, true>(d, q, k, v, o, lse, o_acc, stream)
+                : launch_fwd_t<64, false>(d, q, k, v, o, lse, o_acc, stream);
+  return LOONG_ERR_UNSUPPORTED;
+}
+
+}  // namespace loong

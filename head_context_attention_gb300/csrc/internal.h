@@ -1,0 +1,66 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/loong_attn.h"
+#include "ring.cuh"
+
+namespace loong {
+
+// Records the CUDA error text for loong_last_cuda_error and maps to a status.
+int cuda_fail(cudaError_t e);
+// cudaGetLastError after a launch: LOONG_OK or LOONG_ERR_CUDA.
+int check_launch();
+
+// Optional events recorded around the main attention launches (this thread).
+void record_start(cudaStream_t s);
+void record_stop(cudaStream_t s);
+
+// Device address of the library's error word on the current device.
+unsigned* device_error_word();
+
+// Lazily loaded cuTensorMapEncodeTiled; nullptr if the driver lacks it.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
+
+// bf16 tensor [rows][heads][d] viewed as the 3-D tensor (d, heads, rows),
+// box (64, 1, 128), 128-byte swizzle.  Returns LOONG_OK or an error status.
+int make_head_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d);
+
+RingGeom ring_geom(const loong_attn_desc& d);
+
+// Kernel launchers (asynchronous on `stream`).
+int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
+               float* lse, float* o_acc, cudaStream_t stream);
+int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v,
+               const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+               float* dq_acc, float* dvec, float* dk_acc, float* dv_acc, cudaStream_t stream);
+
+int launch_fill_f32(float* p, int64_t n, float value, cudaStream_t stream);
+int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
+int launch_lse_merge(int64_t rows, int d, int n_parts, const float* o_parts,
+                     const float* lse_parts, void* o_out, float* lse_out, int out_bf16,
+                     cudaStream_t stream);
+int launch_headctx_pack(int64_t batch, int cp, int P, int64_t s_local, int heads, int d,
+                        int direction, int gather, const void* in, void* out,
+                        cudaStream_t stream);
+// Backward row statistics: for every (batch, query head, token) the values
+// LSE*log2(e) and D = rowsum(dO*O), in [B*Hq][stat_row_len] arrays (LSE part
+// first, then D) where block b's tokens start at b*stat_block_pad(blk), so a
+// 128-row tile's statistics are 16-byte aligned and reads past a tile stay in
+// bounds.
+inline int stat_block_pad(int blk) { return (blk + 3) & ~3; }
+inline int64_t stat_row_len(const RingGeom& g) {
+  return static_cast<int64_t>(g.nblocks) * stat_block_pad(g.blk) + kTile;
+}
+int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* dout, const float* lse,
+                        float* stats, cudaStream_t stream);
+
+}  // namespace loong

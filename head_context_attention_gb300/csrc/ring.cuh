@@ -1,0 +1,111 @@
+// ring.cuh -- geometry of the emulated 2D mesh: paired-block (zigzag) or
+// contiguous placement of ring ranks, the inner/outer double-ring step order,
+// and the walk over the key tiles a query tile meets along its ring pass.
+//
+// [G] "Guide to LoongTrain: 2D Head-Context Parallelism for LLMs":
+//   section 2 (Paired-Block Allocation): ring rank r owns blocks r and
+//   2*P_seq-1-r of the 2*P_seq blocks;
+//   "The Communication Overhead and Causal Imbalance of Ring Attention":
+//   query i sees key j only for j <= i.
+// [A] abstract: Double-Ring-Attention; the step order used is the nested one
+//   (one inner-ring hop per step, one outer-ring hop per inner round).
+#pragma once
+
+#include <stdint.h>
+
+namespace loong {
+
+constexpr int kTile = 128;  // rows of a query tile and of a key tile
+
+struct RingGeom {
+  int cp, inner, outer;
+  int zigzag;   // 1 paired blocks, 0 contiguous
+  int blk;      // tokens per block
+  int nblocks;  // blocks per sequence: 2*cp or cp
+  int ntile;    // key/query tiles per block: ceil(blk / 128)
+};
+
+__host__ __device__ inline int ring_src(int c, int t, int inner, int outer) {
+  const int o = t / inner, i = t - (t / inner) * inner;
+  const int g = c / inner, l = c - (c / inner) * inner;
+  return ((g - o + outer) % outer) * inner + (l - i + inner) % inner;
+}
+
+// Ring rank that owns natural block b.
+__host__ __device__ inline int block_owner(const RingGeom& g, int b) {
+  return g.zigzag ? (b < g.cp ? b : 2 * g.cp - 1 - b) : b;
+}
+
+// Natural block index of part `part` (0 = A, 1 = B) of ring rank c.
+__host__ __device__ inline int rank_block(const RingGeom& g, int c, int part) {
+  return part == 0 ? c : 2 * g.cp - 1 - c;
+}
+
+__host__ __device__ inline int rank_parts(const RingGeom& g) { return g.zigzag ? 2 : 1; }
+
+// Key tiles that the query tile (natural block bq, tile qi of that block)
+// meets over ring steps [t0, t1), in ring order: step by step, block A then
+// block B of the step's source rank, tiles in increasing position.  Blocks
+// that lie wholly after bq are skipped; the block bq itself is visited up to
+// the diagonal tile qi.
+struct KvWalk {
+  RingGeom g;
+  int c, bq, qi, t, t1, part, kt, kt_n, bk;
+
+  __host__ __device__ void init(const RingGeom& geom, int bq_, int qi_, int t0, int t1_) {
+    g = geom;
+    bq = bq_;
+    qi = qi_;
+    c = block_owner(g, bq);
+    t = t0;
+    t1 = t1_;
+    part = 0;
+    kt = 0;
+    settle();
+  }
+  __host__ __device__ void settle() {
+    while (t < t1) {
+      const int j = ring_src(c, t, g.inner, g.outer);
+      bk = rank_block(g, j, part);
+      kt_n = bk < bq ? g.ntile : (bk == bq ? qi + 1 : 0);
+      if (kt < kt_n) return;
+      kt = 0;
+      if (++part == rank_parts(g)) {
+        part = 0;
+        ++t;
+      }
+    }
+  }
+  __host__ __device__ bool done() const { return t >= t1; }
+  __host__ __device__ int k0() const { return bk * g.blk + kt * kTile; }
+  __host__ __device__ int klen() const {
+    const int e = (bk + 1) * g.blk - k0();
+    return e < kTile ? e : kTile;
+  }
+  __host__ __device__ bool diag() const { return bk == bq && kt == qi; }
+  __host__ __device__ void advance() {
+    ++kt;
+    settle();
+  }
+  // Number of tiles left, walking a copy.
+  __host__ __device__ int count() const {
+    int n = 0;
+    int tt = t;
+    int pp = part;
+    int first = kt;
+    while (tt < t1) {
+      const int j = ring_src(c, tt, g.inner, g.outer);
+      const int b = rank_block(g, j, pp);
+      const int m = b < bq ? g.ntile : (b == bq ? qi + 1 : 0);
+      if (m > first) n += m - first;
+      first = 0;
+      if (++pp == rank_parts(g)) {
+        pp = 0;
+        ++tt;
+      }
+    }
+    return n;
+  }
+};
+
+}  // namespace loong

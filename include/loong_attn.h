@@ -1,0 +1,225 @@
+/*
+ * loong_attn.h -- C ABI of the GB300 (sm_103a) LoongTrain 2D-Attention ring step.
+ *
+ * One process, one GPU.  Every emulated rank of the head-parallel x
+ * context-parallel mesh lives on this device; a ring "exchange" is the choice
+ * of which K/V chunk a rank reads at a step, so no bytes move between steps.
+ *
+ * Sources (page title, section):
+ *   [G] "Guide to LoongTrain: 2D Head-Context Parallelism for LLMs"
+ *   [A] "LoongTrain: Efficient Training of Long-Sequence LLMs with
+ *       Head-Context Parallelism" (abstract page)
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named q, k, v, o, dout, dq, dk, dv, lse, ws, in, out, o_parts,
+ *     lse_parts, o_out, lse_out are DEVICE pointers owned by the caller.  The
+ *     library allocates no device memory, keeps no state between calls except a
+ *     cached device query, a loaded tensor-map encoder and one device error
+ *     word, and synchronises only in loong_get_device_status.
+ *   - All work is enqueued asynchronously on `stream` (0 = legacy default).
+ *   - Tensors are contiguous.  Q, O, dO, dQ: bf16 [B, S, Hq, d]; K, V, dK, dV:
+ *     bf16 [B, S, Hkv, d], natural token order; LSE: fp32 [B, Hq, S], natural
+ *     log of the softmax denominator of the scaled logits.
+ *   - Base pointers must be 16-byte aligned.
+ *   - Return value: LOONG_OK (0) or a negative loong_status.  No exception
+ *     crosses the ABI; no call aborts the process or traps the GPU.
+ */
+#ifndef LOONG_ATTN_H
+#define LOONG_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LOONG_API __attribute__((visibility("default")))
+#else
+#define LOONG_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* loong_stream_t;
+
+typedef enum {
+  LOONG_OK = 0,
+  LOONG_ERR_INVALID_ARG = -1,     /* null pointer, bad size or divisibility   */
+  LOONG_ERR_WORKSPACE = -2,       /* ws_bytes smaller than the workspace size */
+  LOONG_ERR_UNSUPPORTED = -3,     /* valid but not built: head_dim, non-causal,
+                                     device is not compute capability 10.3    */
+  LOONG_ERR_CUDA = -4,            /* a CUDA call failed; see loong_last_cuda_error */
+  LOONG_ERR_DEVICE_TIMEOUT = -5   /* a kernel's bounded wait expired; the
+                                     kernel stopped early and its outputs are
+                                     undefined                                  */
+} loong_status;
+
+enum { LOONG_PLACEMENT_CONTIGUOUS = 0, LOONG_PLACEMENT_ZIGZAG = 1 };
+enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1 };
+
+/*
+ * Problem descriptor.  Follows the problem statement of [G] "1. 2D Mesh
+ * Topology" (P = P_head x P_seq), "2. Paired-Block Allocation for Causal Load
+ * Balancing" and [A] (Double-Ring-Attention).
+ *   batch, seqlen     B and S (tokens per sequence).
+ *   hq, hkv           query and key/value heads, hq % hkv == 0 (grouped-query
+ *                     attention, [G] "The Scalability Limits of DeepSpeed
+ *                     Ulysses").
+ *   head_dim          d, 64 or 128.
+ *   hp                head-parallel degree P_head: hq % hp == 0 and
+ *                     hkv % hp == 0 (each head rank keeps whole kv heads).
+ *   cp                context-parallel (ring) degree P_seq.
+ *   ring_inner/outer  double-ring shape, inner * outer == cp.  At step
+ *                     t = o*inner + i ring rank c holds the K/V of rank
+ *                     ((c/inner - o) mod outer)*inner + ((c%inner - i) mod inner).
+ *   causal            must be 1 (query i sees key j only for j <= i, [G] "The
+ *                     Communication Overhead and Causal Imbalance of Ring
+ *                     Attention").
+ *   placement         LOONG_PLACEMENT_ZIGZAG: ring rank r owns blocks r and
+ *                     2cp-1-r of length S/(2cp); CONTIGUOUS: block r of length
+ *                     S/cp.  The block length must be a multiple of hp.
+ *   mode              LOONG_MODE_FUSED: one launch walks all ring steps and
+ *                     keeps the running softmax on chip; STEPWISE: one launch
+ *                     per ring step, each merging its partial result into an
+ *                     fp32 accumulator by log-sum-exp.
+ *   softmax_scale     <= 0 selects 1/sqrt(head_dim) ([G] "Step 3",
+ *                     forward_local_attention).
+ */
+typedef struct {
+  int64_t batch, seqlen;
+  int32_t hq, hkv, head_dim;
+  int32_t hp, cp, ring_inner, ring_outer;
+  int32_t causal;
+  int32_t placement;
+  int32_t mode;
+  float softmax_scale;
+} loong_attn_desc;
+
+/* Library version, (major << 16) | minor. */
+LOONG_API int loong_version(void);
+
+/* Human-readable text for a loong_status value (static storage). */
+LOONG_API const char* loong_status_string(int status);
+
+/* Text of the last CUDA error seen by this library in this thread (static). */
+LOONG_API const char* loong_last_cuda_error(void);
+
+/*
+ * Check a descriptor without touching the GPU.  Returns LOONG_OK,
+ * LOONG_ERR_INVALID_ARG or LOONG_ERR_UNSUPPORTED (see loong_attn_desc).
+ */
+LOONG_API int loong_attn_check(const loong_attn_desc* desc);
+
+/*
+ * Device workspace, in bytes, that loong_attn_fwd (pass 0) or loong_attn_bwd
+ * (pass 1) needs for `desc`; 0 for an invalid descriptor.  Host-only.
+ *   fwd, FUSED: 0.  fwd, STEPWISE: fp32 O accumulator [B,S,Hq,d].
+ *   bwd: fp32 dQ accumulator [B,S,Hq,d] + fp32 row statistics (LSE*log2 e
+ *        and D = rowsum(dO*O)), 2 x B x Hq x (nblocks*roundup(blk,4) + 128)
+ *        values, with nblocks = 2cp (ZIGZAG) or cp and blk = S/nblocks;
+ *        STEPWISE adds fp32 dK, dV accumulators [B,S,Hkv,d] each.
+ *   Each part starts on a 256-byte boundary.
+ */
+LOONG_API size_t loong_attn_workspace_size(const loong_attn_desc* desc, int pass);
+
+/*
+ * The ring schedule as a host table: src[t * cp + c] = ring rank whose K/V
+ * ring rank c holds at step t (double-ring reading above).  src must hold
+ * inner*outer*inner*outer int32.  Host-only.
+ */
+LOONG_API int loong_ring_schedule(int32_t ring_inner, int32_t ring_outer, int32_t* src);
+
+/*
+ * Forward ring attention ([G] "Step 3", forward_local_attention per block
+ * pair, merged over the ring steps).  For every emulated rank (ring rank c,
+ * head rank h), every ring step t and every query head of head group h,
+ * computes causal softmax attention of rank c's query blocks against the K/V
+ * blocks of rank src(c, t) and merges the step's result into the running
+ * result by log-sum-exp.  The result equals causal attention over the whole
+ * sequence up to rounding.
+ *   q, k, v   inputs (layouts above), read only.
+ *   o         bf16 output [B,S,Hq,d].
+ *   lse       fp32 output [B,Hq,S].
+ *   ws        device workspace of at least loong_attn_workspace_size(desc,0)
+ *             bytes (may be NULL when that size is 0).
+ */
+LOONG_API int loong_attn_fwd(const loong_attn_desc* desc, const void* q, const void* k, const void* v,
+                   void* o, float* lse, void* ws, size_t ws_bytes, loong_stream_t stream);
+
+/*
+ * Backward of loong_attn_fwd: the exact gradient of causal softmax attention
+ * (the pages give no backward; this is the plain chain rule through softmax).
+ * Over the same schedule: P = exp(s - LSE), dV += P^T dO, dP = dO V^T,
+ * dS = P * (dP - D) with D = rowsum(dO * O), dQ += scale dS K,
+ * dK += scale dS^T Q; dK and dV sum over the query heads of a kv group.
+ *   o, lse    the outputs of loong_attn_fwd for the same inputs.
+ *   dout      bf16 dO [B,S,Hq,d].
+ *   dq        bf16 [B,S,Hq,d]; dk, dv bf16 [B,S,Hkv,d]; written, not added to.
+ *   ws        at least loong_attn_workspace_size(desc,1) bytes.
+ */
+LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const void* k, const void* v,
+                   const void* o, const float* lse, const void* dout,
+                   void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                   loong_stream_t stream);
+
+/*
+ * n-way log-sum-exp merge of partial attention results over disjoint key sets
+ * (the pages leave the merge implicit; it is the rule under which softmax over
+ * a union of key sets is recovered from the parts):
+ *   L = ln sum_p exp(L_p),  O = sum_p exp(L_p - L) O_p.
+ * A part with L_p = -inf is empty and has weight 0; if all parts are empty the
+ * row gets L = -inf and O = 0.
+ *   o_parts   fp32 [n_parts][rows][d];  lse_parts fp32 [n_parts][rows].
+ *   o_out     fp32 [rows][d] (out_bf16 == 0) or bf16 [rows][d] (out_bf16 == 1).
+ *   lse_out   fp32 [rows].
+ * rows >= 0 (0 is a no-op), 1 <= d <= 1024 with d % 4 == 0, 1 <= n_parts <= 64.
+ * Outputs must not overlap inputs.
+ */
+LOONG_API int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts,
+                    const float* o_parts, const float* lse_parts,
+                    void* o_out, float* lse_out, int out_bf16, loong_stream_t stream);
+
+/*
+ * Ulysses head-context repack ([G] "The Scalability Limits of DeepSpeed
+ * Ulysses": all-to-all (S/P, H) -> (S, H/P) before attention and the inverse
+ * after), for every ring rank's head-parallel group at once, as a bit copy of
+ * 2-byte elements.
+ *   direction 0:  out[n][p][q*s_local + t][h'][:] = in[n][q][t][p*H/P + h'][:]
+ *   direction 1:  the inverse (out and in swap roles).
+ * with n < batch*cp (group = ring rank of one sequence), p, q < P, t < s_local,
+ * h' < H/P.  `gather` selects the layout of the (S/P, H) side:
+ *   0  rank-major [batch*cp][P][s_local][H][d];
+ *   1  natural token order [batch][S][H][d], S = cp*P*s_local, ring rank n
+ *      owning the paired blocks n and 2cp-1-n ([G] section 2);
+ *   2  natural token order with contiguous blocks.
+ * The (S, H/P) side is always rank-major [batch*cp][P][P*s_local][H/P][d].
+ * H % P == 0, d*2 bytes a multiple of 16, in and out must not overlap.
+ */
+LOONG_API int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s_local, int32_t heads,
+                       int32_t d, int direction, int gather, const void* in, void* out,
+                       loong_stream_t stream);
+
+/*
+ * Measurement aid.  When both are non-NULL, the calling thread's next
+ * loong_attn_fwd / loong_attn_bwd calls record `start_event` on their stream
+ * just before launching the main ring-attention kernel(s) and `stop_event`
+ * just after the last of them, so the kernels' device time can be read with
+ * cudaEventElapsedTime without counting the call's helper kernels.  The events
+ * are cudaEvent_t handles owned by the caller; pass NULL, NULL to stop.
+ */
+LOONG_API int loong_set_timing_events(void* start_event, void* stop_event);
+
+/*
+ * Synchronise `stream` and report device-side failures of earlier calls:
+ * LOONG_ERR_DEVICE_TIMEOUT if a kernel's bounded wait expired (the error word
+ * is then cleared), LOONG_ERR_CUDA if the stream reports a CUDA error,
+ * LOONG_OK otherwise.
+ */
+LOONG_API int loong_get_device_status(loong_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOONG_ATTN_H */

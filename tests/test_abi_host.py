@@ -1,0 +1,111 @@
+"""Host-side checks of the C-ABI library: it loads without a GPU, exports every
+declared symbol, validates descriptors, sizes workspaces and produces the ring
+table the oracle defines.  No compute call is made."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from head_context_attention_gb300 import inputs, ops
+from oracle import schedule
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            with open(os.path.join(inc, f)) as fh:
+                names |= set(re.findall(r"LOONG_API\s+[\w\s\*]+?\b(loong_\w+)\s*\(", fh.read()))
+    return names
+
+
+def test_library_exports_every_declared_symbol(loong_lib):
+    names = _declared()
+    assert len(names) >= 11
+    assert names == set(ops.EXPORTS)
+    for n in names:
+        assert hasattr(loong_lib, n), n
+
+
+def test_status_strings(loong_lib):
+    for st in (0, -1, -2, -3, -4, -5):
+        assert ops.lib().loong_status_string(st)
+    assert ops.lib().loong_version() >= 1
+
+
+@pytest.mark.parametrize("inner,outer", [(4, 1), (4, 2), (8, 2), (8, 4), (8, 8), (3, 5)])
+def test_ring_schedule_matches_oracle(loong_lib, inner, outer):
+    got = np.array(ops.loong_ring_schedule(inner, outer))
+    np.testing.assert_array_equal(got, schedule.schedule_table(inner, outer))
+
+
+def _desc(**kw):
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    d = ops.make_desc(w)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("hq", 30, ops.LOONG_ERR_INVALID_ARG),          # Hq % Hkv
+    ("hp", 16, ops.LOONG_ERR_INVALID_ARG),          # Hkv % hp: a kv head would be split
+    ("ring_inner", 4, ops.LOONG_ERR_INVALID_ARG),   # inner * outer != cp
+    ("seqlen", 131072 + 32, ops.LOONG_ERR_INVALID_ARG),  # S % (2 cp)
+    ("head_dim", 96, ops.LOONG_ERR_UNSUPPORTED),
+    ("causal", 0, ops.LOONG_ERR_UNSUPPORTED),
+    ("placement", 7, ops.LOONG_ERR_INVALID_ARG),
+    ("mode", 3, ops.LOONG_ERR_INVALID_ARG),
+    ("batch", 0, ops.LOONG_ERR_INVALID_ARG),
+])
+def test_descriptor_validation(loong_lib, field, value, status):
+    assert ops.loong_attn_check(_desc()) == ops.LOONG_OK
+    assert ops.loong_attn_check(_desc(**{field: value})) == status
+
+
+def test_block_length_must_split_over_hp(loong_lib):
+    # S = 2*cp*blk with blk = 12 and hp = 8: the Ulysses split of a block fails
+    d = _desc(seqlen=2 * 16 * 12)
+    assert ops.loong_attn_check(d) == ops.LOONG_ERR_INVALID_ARG
+    d = _desc(seqlen=2 * 16 * 16)
+    assert ops.loong_attn_check(d) == ops.LOONG_OK
+
+
+def test_workspace_sizes(loong_lib):
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    fused, step = ops.make_desc(w, ops.MODE_FUSED), ops.make_desc(w, ops.MODE_STEPWISE)
+    q_el = w.seqlen * w.hq * w.head_dim
+    kv_el = w.seqlen * w.hkv * w.head_dim
+    assert ops.loong_attn_workspace_size(fused, 0) == 0
+    assert ops.loong_attn_workspace_size(step, 0) == q_el * 4
+    blk = w.seqlen // (2 * w.cp)
+    stats = 2 * w.hq * (2 * w.cp * ((blk + 3) // 4 * 4) + 128) * 4
+    up = lambda x: (x + 255) // 256 * 256
+    assert ops.loong_attn_workspace_size(fused, 1) == up(q_el * 4) + up(stats)
+    assert ops.loong_attn_workspace_size(step, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
+    bad = _desc(hq=30)
+    assert ops.loong_attn_workspace_size(bad, 0) == 0
+
+
+def test_null_pointers_rejected_before_any_cuda_call(loong_lib):
+    d = _desc()
+    L = ops.lib()
+    assert L.loong_attn_fwd(ctypes.byref(d), None, None, None, None, None, None, 0, None) == \
+        ops.LOONG_ERR_INVALID_ARG
+    assert L.loong_lse_merge(10, 3, 2, None, None, None, None, 0, None) == ops.LOONG_ERR_INVALID_ARG
+    assert L.loong_lse_merge(0, 128, 2, None, None, None, None, 0, None) == ops.LOONG_OK
+    assert L.loong_headctx_pack(1, 2, 3, 4, 8, 128, 0, 0, None, None, None) == \
+        ops.LOONG_ERR_INVALID_ARG   # heads % P
+    assert L.loong_headctx_pack(0, 2, 2, 4, 8, 128, 0, 0, None, None, None) == ops.LOONG_OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(ops, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        ops.lib()

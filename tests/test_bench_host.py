@@ -1,0 +1,75 @@
+"""Host-side logic of bench.py: clock-record parsing, the max-over-ranks
+timing reduction on world_size 2 (gloo, CPU) and the reference arm's JSON."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_clock_summary_parses_reasons():
+    c = bench.ClockSampler(0)
+    c.lines = ["0, 1900, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Active",
+               "0, 1950, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1800, 2070, 980.0, 0x0, Not Active, Active, Not Active, Not Active",
+               "garbage"]
+    s = c.summary()
+    assert s["sm_mhz"] == 1900 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2")
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    v = bench.max_over_ranks(dist, 10.0 + rank * 5.0, "cpu")
+    bench.barrier(dist)
+    q.put((rank, v))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_world2_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+    assert got == {0: 15.0, 1: 15.0}
+
+
+def test_reference_arm_prints_one_json_line(tmp_path):
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0", "--workload", "tiny-gqa-s1k",
+                        "--cpu-seconds", "1"], capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_nonzero_rank_exits_quietly():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True, env=env,
+                       timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
