@@ -288,11 +288,13 @@ __global__ void __launch_bounds__(320, 1)
         }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       const float m_new = fmaxf(m_run, m_tile);
-      if (j == 0) {
-        m_run = m_new;
-      } else if (m_new > m_run + kRescaleThreshold) {
+      const bool rescale = j > 0 && m_new > m_run + kRescaleThreshold;
+      if (j == 0) m_run = m_new;
+      // The decision is per row, but TMEM loads and stores are warp-collective:
+      // the whole warp takes the branch, rows that need none scale by 1.
+      if (__any_sync(0xffffffffu, rescale)) {
         // O_h is stable: the commit that signalled S_h follows O_h += P V.
-        const float f = fast_exp2(m_run - m_new);
+        const float f = rescale ? fast_exp2(m_run - m_new) : 1.f;
         l_run *= f;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
           tmem_st32(tO + cb * 32, orow);
         }
-        m_run = m_new;
+        if (rescale) m_run = m_new;
       }
       const float ref = m_run == -INFINITY ? 0.f : m_run;
       float l0 = 0.f, l1 = 0.f;

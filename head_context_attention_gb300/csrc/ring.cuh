@@ -108,4 +108,79 @@ struct KvWalk {
   }
 };
 
+// Ring rank that holds source j's K/V at step t (inverse of ring_src in c).
+__host__ __device__ inline int ring_dst(int j, int t, int inner, int outer) {
+  const int o = t / inner, i = t - (t / inner) * inner;
+  const int g = j / inner, l = j - (j / inner) * inner;
+  return ((g + o) % outer) * inner + (l + i) % inner;
+}
+
+// The (query tile, head) pairs that meet key tile (block bk, tile kt) over
+// ring steps [t0, t1), in the order the K/V chunk visits ranks.
+struct QWalk {
+  RingGeom g;
+  int G, bk, kt, j, t, t1, part, qi, qi_end, head, bq;
+
+  __host__ __device__ void init(const RingGeom& geom, int G_, int bk_, int kt_, int t0, int t1_) {
+    g = geom;
+    G = G_;
+    bk = bk_;
+    kt = kt_;
+    j = block_owner(g, bk);
+    t = t0;
+    t1 = t1_;
+    part = 0;
+    qi = -1;
+    head = 0;
+    next_block();
+  }
+  // Position on the first query tile of the next block that sees bk.
+  __host__ __device__ void next_block() {
+    while (t < t1) {
+      if (qi < 0) {
+        const int c = ring_dst(j, t, g.inner, g.outer);
+        bq = rank_block(g, c, part);
+        qi_end = g.ntile;
+        qi = bk < bq ? 0 : (bk == bq ? kt : g.ntile);
+        if (qi < qi_end) return;
+      }
+      qi = -1;
+      if (++part == rank_parts(g)) {
+        part = 0;
+        ++t;
+      }
+    }
+  }
+  __host__ __device__ bool done() const { return t >= t1; }
+  __host__ __device__ void advance() {
+    if (++head < G) return;
+    head = 0;
+    if (++qi < qi_end) return;
+    qi = -1;
+    if (++part == rank_parts(g)) {
+      part = 0;
+      ++t;
+    }
+    next_block();
+  }
+  __host__ __device__ int q0() const { return bq * g.blk + qi * kTile; }
+  __host__ __device__ int qlen() const {
+    const int e = (bq + 1) * g.blk - q0();
+    return e < kTile ? e : kTile;
+  }
+  __host__ __device__ bool diag() const { return bq == bk && qi == kt; }
+  __host__ __device__ int count() const {
+    int n = 0;
+    for (int tt = t; tt < t1; ++tt) {
+      const int c = ring_dst(j, tt, g.inner, g.outer);
+      for (int pp = 0; pp < rank_parts(g); ++pp) {
+        const int b = rank_block(g, c, pp);
+        if (bk < b) n += g.ntile;
+        else if (bk == b) n += g.ntile - kt;
+      }
+    }
+    return n * G;
+  }
+};
+
 }  // namespace loong

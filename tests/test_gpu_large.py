@@ -1,0 +1,88 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py
+times (FUSED mode): the oracle recomputes sampled outputs one by one.
+
+  * O, LSE and dQ on >= 512 query rows of two heads (row 0, the first and last
+    row of every paired block, random rows), each from its own O(S d) softmax;
+  * dK, dV on sampled keys of one kv head from the last positions (they need
+    only the queries after them);
+  * over all keys: sum_j dK_j = 0 and sum_j dV_j = sum of dO over the group's
+    query heads (rows of dS sum to 0, rows of P to 1).
+Parity beyond these samples rests on the small-size element-wise tests.
+"""
+import numpy as np
+import pytest
+import torch
+
+from head_context_attention_gb300 import inputs, ops
+from oracle import attention
+from tests.helpers import assert_close
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+KEYS_TAIL = {"llama3-8b-s32k-fwd": 0, "llama3-8b-s128k": 1024, "llama3-70b-s256k": 512,
+             "headgroup-s1m-peaky": 128}
+
+
+def _sample_rows(w, rng, n=512):
+    nb = 2 * w.cp
+    blk = w.seqlen // nb
+    rows = {0, w.seqlen - 1}
+    for b in range(nb):
+        rows.add(b * blk)
+        rows.add(b * blk + blk - 1)
+    while len(rows) < n:
+        rows.add(int(rng.integers(0, w.seqlen)))
+    return np.array(sorted(rows))
+
+
+def _head_arrays(x, key, heads):
+    return {h: x[key][0, :, h].to("cpu", torch.float64).numpy() for h in heads}
+
+
+@pytest.mark.parametrize("name", ["llama3-8b-s32k-fwd", "llama3-8b-s128k", "llama3-70b-s256k",
+                                  "headgroup-s1m-peaky"])
+def test_full_size_sampled_parity(cuda_device, name):
+    w = inputs.WORKLOADS[name]
+    x = inputs.make_inputs(w, device="cuda", with_do=True)
+    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    if w.backward:
+        dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"])
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    rng = np.random.default_rng(7)
+    rows = _sample_rows(w, rng)
+    G = w.hq // w.hkv
+    heads = [0, w.hq - 1]
+    f64 = lambda t: t.to("cpu", torch.float64).numpy()
+    for h in heads:
+        g = h // G
+        q = f64(x["q"][0, :, h:h + 1])
+        k = f64(x["k"][0, :, g:g + 1])
+        v = f64(x["v"][0, :, g:g + 1])
+        ro, rl = attention.attention_rows(q, k, v, rows, [0])
+        assert_close(f"O h{h}", f64(o[0, rows, h]), ro[0], 2e-2, 2e-2)
+        assert_close(f"LSE h{h}", f64(lse[0, h, rows]), rl[0], 1e-3, 0.0)
+        if w.backward:
+            do = f64(x["do"][0, :, h:h + 1])
+            rdq = attention.attention_backward_rows(q, k, v, do, rows, [0])
+            assert_close(f"dQ h{h}", f64(dq[0, rows, h]), rdq[0], 5e-2, 5e-2)
+    if not w.backward:
+        return
+    # sampled keys of the last kv head, from the tail of the sequence
+    g = w.hkv - 1
+    tail = KEYS_TAIL[name]
+    keys = np.unique(np.concatenate([rng.integers(w.seqlen - tail, w.seqlen, size=24),
+                                     [w.seqlen - tail, w.seqlen - 1]]))
+    qh = slice(g * G, (g + 1) * G)
+    q = f64(x["q"][0, :, qh])
+    do = f64(x["do"][0, :, qh])
+    k = f64(x["k"][0, :, g:g + 1])
+    v = f64(x["v"][0, :, g:g + 1])
+    sk, sv = attention.attention_backward_keys(q, k, v, do, keys, kv_head=0)
+    assert_close("dK keys", f64(dk[0, keys, g]), sk, 5e-2, 5e-2)
+    assert_close("dV keys", f64(dv[0, keys, g]), sv, 5e-2, 5e-2)
+    # invariants over every key
+    dk_sum = dk[0].double().sum(dim=0).cpu().numpy()
+    scale = float(np.abs(dk[0].double().cpu().numpy()).sum(axis=0).max())
+    assert np.abs(dk_sum).max() < 2e-3 * scale + 1.0
+    do_grp = x["do"][0].double().reshape(w.seqlen, w.hkv, G, w.head_dim).sum(dim=(0, 2)).cpu().numpy()
+    assert_close("sum dV", dv[0].double().sum(dim=0).cpu().numpy(), do_grp, 2.0, 1e-2)
