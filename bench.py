@@ -43,6 +43,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--seqlen", type=int, default=0,
+                   help="override S (a smaller case of the same shape, e.g. for profiler captures)")
+    p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
     return p.parse_args(argv)
 
 
@@ -231,13 +234,16 @@ def run_gpu(args, w, rank, local, world, pg):
             ops.loong_headctx_pack(t, packed[n], w.batch, w.cp, P, s_local, t.shape[2], w.head_dim, 0, 1,
                                    stream)
 
+    do_bwd = w.backward
+
     def step():
         repack()
         ops.loong_attn_fwd(desc, q, k, v, o, lse, ws0, stream)
-        ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
+        if do_bwd:
+            ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
 
     launches_per_step = 3 + (1 if mode == ops.MODE_FUSED else w.cp + 2) + \
-        (3 if mode == ops.MODE_FUSED else w.cp + 4)
+        ((3 if mode == ops.MODE_FUSED else w.cp + 4) if do_bwd else 0)
 
     for _ in range(args.warmup):
         step()
@@ -261,8 +267,9 @@ def run_gpu(args, w, rank, local, world, pg):
             ev_p[i][1].record(stream)
             ops.loong_set_timing_events(*ev_f[i])
             ops.loong_attn_fwd(desc, q, k, v, o, lse, ws0, stream)
-            ops.loong_set_timing_events(*ev_b[i])
-            ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
+            if do_bwd:
+                ops.loong_set_timing_events(*ev_b[i])
+                ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
             ops.loong_set_timing_events(None, None)
         t_stop.record(stream)
         torch.cuda.synchronize(dev)
@@ -274,14 +281,14 @@ def run_gpu(args, w, rank, local, world, pg):
     ms_total = max_over_ranks(pg, ms_total, dev)
     ms_step = ms_total / args.steps
     f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
-    b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b)
+    b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b) if do_bwd else 0.0
     p_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_p)
     peaks = measured_peaks()
     flops_step = w.flops
     tflops = flops_step * world / (ms_step * 1e-3) / 1e12
 
     bwd_flops = w.fwd_flops * 2.5
-    bwd_tf = bwd_flops / (b_ms * 1e-3) / 1e12
+    bwd_tf = bwd_flops / (b_ms * 1e-3) / 1e12 if do_bwd else 0.0
     fwd_tf = w.fwd_flops / (f_ms * 1e-3) / 1e12
     pack_bytes = 2 * w.batch * w.seqlen * (w.hq + 2 * w.hkv) * w.head_dim * 2
     pack_gbs = pack_bytes / (p_ms * 1e-3) / 1e9
@@ -320,6 +327,9 @@ def run_gpu(args, w, rank, local, world, pg):
     if rejected:
         result["clocks"]["rejected"] = rejected
 
+    if not do_bwd:
+        del result["kernels"]["ring_bwd_kernel"]
+        result["config"]["pass"] = "forward only"
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, w, desc, dev, stream, world, pg, x)
     return result, x
@@ -348,8 +358,9 @@ def run_e2e(args, w, desc, dev, stream, world, pg, x):
         for n in dev_in:
             dev_in[n].copy_(host_in[n], non_blocking=True)
         ops.loong_attn_fwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, ws0, stream)
-        ops.loong_attn_bwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, dev_in["do"], dq, dk, dv, ws1,
-                           stream)
+        if w.backward:
+            ops.loong_attn_bwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, dev_in["do"], dq, dk, dv,
+                               ws1, stream)
         for n in host_out:
             host_out[n].copy_(outs[n], non_blocking=True)
 
@@ -375,8 +386,9 @@ def main(argv=None):
     if args.workload not in inputs.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; one of {sorted(inputs.WORKLOADS)}")
     w = inputs.WORKLOADS[args.workload]
-    if not w.backward:
-        w = w.with_(backward=True)
+    if args.seqlen:
+        w = w.with_(seqlen=args.seqlen, name=f"{w.name}@S={args.seqlen}")
+    w = w.with_(backward=not args.fwd_only)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 

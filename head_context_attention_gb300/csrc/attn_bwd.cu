@@ -19,8 +19,10 @@
 // all 128 TMEM lanes; group w handles query columns [64w, 64w+64) of S^T/dP^T
 // and head-dim columns [D/2*w, D/2*(w+1)) of dQ; warp 8 issues TMA loads,
 // warp 9 allocates TMEM and issues the MMAs.
-// Tensor memory (512 columns): R0 [0,128) S^T then P^T (bf16 pairs, first 64
-// columns); R1 [128,256) dP^T then dQ; dV and dK after that (D columns each).
+// Tensor memory (512 columns): R0 [0,128) S^T, then P^T as bf16 pairs, each
+// group packing its 64 queries into the first 32 columns of its own half (the
+// two groups share lanes, so neither may write where the other still reads);
+// R1 [128,256) dP^T then dQ; dV and dK after that (D columns each).
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -202,11 +204,12 @@ __global__ void __launch_bounds__(320, 1)
           if (!mbar_wait(pd_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           const uint32_t qs = q_addr + s * C::TILE_BYTES, os = o_addr + s * C::TILE_BYTES;
-          // dV += P^T dO: A = P^T (TMEM, 8 columns per 16 queries), B = dO MN-major
+          // dV += P^T dO: A = P^T (TMEM, 8 columns per 16 queries; queries 64..127
+          // start at column 64), B = dO MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tbase + C::RV, tbase + C::R0 + kk * 8, sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv,
-                   i > 0 || kk > 0);
+            mma_ts(tbase + C::RV, tbase + C::R0 + (kk >> 2) * 64 + (kk & 3) * 8,
+                   sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, i > 0 || kk > 0);
           // dK += dS^T Q: A = dS^T K-major (queries contiguous), B = Q MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -291,10 +294,11 @@ __global__ void __launch_bounds__(320, 1)
           dsk[e / 2] = pack_bf16(ds[0], ds[1]);
           dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
         }
-        // P^T (bf16 pairs) into R0 columns [cbase/2, cbase/2 + 16)
+        // P^T (bf16 pairs) into this group's own half of R0, columns
+        // [64 grp + 16 ch, +16): already read by this group, never read by the other.
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tbase + t_lane + C::R0 + cbase / 2),
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tbase + t_lane + C::R0 + grp * 64 + ch * 16),
             "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]),
             "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
             : "memory");

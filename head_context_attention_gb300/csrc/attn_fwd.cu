@@ -62,6 +62,9 @@ struct FwdArgs {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Of every 8 consecutive score columns, this many take their exponential on
+// the FMA pipe (exp2_fma) instead of the MUFU unit.
+constexpr int kFmaExpPer8 = 0;
 
 template <int D, bool STEP>
 __global__ void __launch_bounds__(320, 1)
@@ -314,8 +317,10 @@ __global__ void __launch_bounds__(320, 1)
       for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[cb][i]), sl2, -ref));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[cb][i + 1]), sl2, -ref));
+          const float x0 = fmaf(__uint_as_float(sr[cb][i]), sl2, -ref);
+          const float x1 = fmaf(__uint_as_float(sr[cb][i + 1]), sl2, -ref);
+          const float p0 = (i & 7) < kFmaExpPer8 ? exp2_fma(x0) : fast_exp2(x0);
+          const float p1 = ((i + 1) & 7) < kFmaExpPer8 ? exp2_fma(x1) : fast_exp2(x1);
           l0 += p0;
           l1 += p1;
           pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);

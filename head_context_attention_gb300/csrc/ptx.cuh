@@ -222,6 +222,25 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// 2^x on the FMA pipe, for offloading part of the softmax exponentials from
+// the MUFU unit.  Cody-Waite style reduction: n = round(x) (the 1.5*2^23 shift
+// leaves n in the low mantissa bits), f = x - n in [-1/2, 1/2], 2^f from a
+// degree-3 polynomial with constant term 1 whose coefficients are a discrete
+// minimax fit of the relative error (fit_exp2_poly.py), and 2^n added into the
+// exponent field.  Relative error <= 1.1e-4 for x in [-126, 8], below the
+// 2^-9 rounding of the bf16 probabilities it feeds.  x <= -127 (including
+// -inf) returns +0.
+__device__ __forceinline__ float exp2_fma(float x) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  constexpr float c1 = 6.932829022e-01f, c2 = 2.422109693e-01f, c3 = 5.500905961e-02f;
+  x = fmaxf(x, -127.0f);
+  const float t = x + kShift;
+  const float f = x - (t - kShift);
+  const float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, 1.0f);
+  const int n = __float_as_int(t) - __float_as_int(kShift);
+  return __int_as_float(__float_as_int(p) + (n << 23));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

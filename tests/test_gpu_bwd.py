@@ -43,11 +43,16 @@ def _run(w, mode):
 def test_backward_matches_oracle(cuda_device, name, mode):
     w = _workload(name)
     x, grads = _run(w, mode)
+    errors = []
     for b in range(w.batch):
         want = attention.attention_backward(to64(x["q"][b]), to64(x["k"][b]), to64(x["v"][b]),
                                             to64(x["do"][b]))[:3]
         for nm, got, exp in zip(("dQ", "dK", "dV"), grads, want):
-            assert_close(nm, to64(got[b]), exp, ATOL, RTOL)
+            try:
+                assert_close(nm, to64(got[b]), exp, ATOL, RTOL)
+            except AssertionError as e:
+                errors.append(str(e))
+    assert not errors, "\n".join(errors)
 
 
 def test_backward_gradient_sums(cuda_device):
