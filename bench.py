@@ -257,6 +257,11 @@ def run_gpu(args, w, rank, local, world, pg):
     ev_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # torch creates events lazily and tracks recording itself: record each once
+    # here so the handle exists (the library re-records it around its kernels).
+    for a, b in ev_f + ev_b:
+        a.record(stream)
+        b.record(stream)
     barrier(pg)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:

@@ -147,7 +147,9 @@ def loong_headctx_pack(x, out, batch, cp, P, s_local, heads, d, direction, gathe
 
 def loong_set_timing_events(start=None, stop=None):
     """Record torch.cuda.Event ``start``/``stop`` around the main attention
-    kernels of this thread's next fwd/bwd calls (None, None to stop)."""
+    kernels of this thread's next fwd/bwd calls (None, None to stop).  torch
+    creates an event on its first record(), so record both once before
+    passing them."""
     sp = None if start is None else ctypes.c_void_p(start.cuda_event)
     ep = None if stop is None else ctypes.c_void_p(stop.cuda_event)
     return _check("loong_set_timing_events", lib().loong_set_timing_events(sp, ep))
