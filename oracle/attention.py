@@ -16,7 +16,9 @@ Readings where the pages are silent:
   * The backward pass is the exact gradient of the forward pass: with
     D_i = dO_i . O_i, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K,
     dK = scale dS^T Q, dV = P^T dO, with dK and dV summed over the query heads
-    that share a kv head.
+    that share a kv head.  Optionally (``d_from_bf16_o``) D is formed from O
+    rounded to bf16, the output the forward returns; with peaky logits this
+    rounding moves dQ by up to ~0.1 (keys scaled x8 at S = 1M).
 
 Layouts: q [S, Hq, d], k and v [S, Hkv, d], o [S, Hq, d], lse [Hq, S].  The
 batch dimension is handled by the caller (B = 1 in every workload).
@@ -26,6 +28,32 @@ import numpy as np
 
 def _f64(x):
     return np.asarray(x, dtype=np.float64)
+
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 value (ties to even), returned as float64.
+
+    bfloat16 is the upper half of an IEEE-754 binary32: the value is first
+    rounded to binary32 (numpy, ties to even), then its low 16 bits are
+    removed with round-to-nearest-even on the bit pattern.  Inf and NaN pass
+    through (no input here is either).
+    """
+    f = np.asarray(x, dtype=np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _dvec(do, o, d_from_bf16_o):
+    """D_i = dO_i . O_i; with ``d_from_bf16_o`` O is first rounded to bf16.
+
+    Reading taken for the backward: D is formed from the output the forward
+    returns, which is O rounded to bf16; ``d_from_bf16_o=False`` gives the
+    exact gradient of the unrounded forward.
+    """
+    if d_from_bf16_o:
+        o = round_bf16(o)
+    return np.einsum("...d,...d->...", do, o)
 
 
 def group_size(hq, hkv):
@@ -63,11 +91,12 @@ def attention_forward(q, k, v, scale=None, causal=True):
     return o, lse
 
 
-def attention_backward(q, k, v, do, scale=None, causal=True):
+def attention_backward(q, k, v, do, scale=None, causal=True, d_from_bf16_o=False):
     """Full backward: returns (dq, dk, dv, o, lse, D) in float64.
 
     Recomputes the forward from its definition, then applies the chain rule
     through softmax (dS = P * (dP - D), D_i = sum_j P_ij dP_ij = dO_i . O_i).
+    ``d_from_bf16_o``: see ``_dvec``.
     """
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
     sq, hq, d = q.shape
@@ -79,7 +108,7 @@ def attention_backward(q, k, v, do, scale=None, causal=True):
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
-    dvec = np.einsum("shd,shd->hs", do, o)
+    dvec = _dvec(do, o, d_from_bf16_o).T
     if causal:
         future = np.arange(sk)[None, :] > np.arange(sq)[:, None]
     for h in range(hq):
@@ -130,7 +159,7 @@ def attention_rows(q, k, v, rows, heads, scale=None):
     return o, lse
 
 
-def attention_backward_rows(q, k, v, do, rows, heads, scale=None):
+def attention_backward_rows(q, k, v, do, rows, heads, scale=None, d_from_bf16_o=False):
     """dQ for selected query rows of selected heads (causal).
 
     dQ_i = scale * sum_{j<=i} P_ij (dP_ij - D_i) k_j with D_i = dO_i . O_i,
@@ -155,14 +184,14 @@ def attention_backward_rows(q, k, v, do, rows, heads, scale=None):
             s = scale * (q[rr, h, :] @ kh[:n].T)
             s = np.where(np.arange(n)[None, :] > rr[:, None], -np.inf, s)
             p = np.exp(s - lse[a, r0:r0 + group][:, None])
-            dvec = np.einsum("rd,rd->r", do[rr, h, :], o[a, r0:r0 + group])
+            dvec = _dvec(do[rr, h, :], o[a, r0:r0 + group], d_from_bf16_o)
             dp = do[rr, h, :] @ vh[:n].T
             ds = p * (dp - dvec[:, None])
             dq[a, r0:r0 + group] = scale * (ds @ kh[:n])
     return dq
 
 
-def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None):
+def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None, d_from_bf16_o=False):
     """dK and dV for selected key positions of one kv head (causal).
 
     dV_j = sum_{h in group} sum_{i>=j} P_ij dO_i and
@@ -187,7 +216,7 @@ def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None):
     for a, h in enumerate(heads):
         qh = q[rows, h, :]
         doh = do[rows, h, :]
-        dvec = np.einsum("rd,rd->r", doh, o[a])
+        dvec = _dvec(doh, o[a], d_from_bf16_o)
         s = scale * (qh @ kj.T)
         s = np.where(keys[None, :] > rows[:, None], -np.inf, s)
         p = np.exp(s - lse[a][:, None])

@@ -63,7 +63,7 @@ def test_full_size_sampled_parity(cuda_device, name):
         assert_close(f"LSE h{h}", f64(lse[0, h, rows]), rl[0], 1e-3, 0.0)
         if w.backward:
             do = f64(x["do"][0, :, h:h + 1])
-            rdq = attention.attention_backward_rows(q, k, v, do, rows, [0])
+            rdq = attention.attention_backward_rows(q, k, v, do, rows, [0], d_from_bf16_o=True)
             assert_close(f"dQ h{h}", f64(dq[0, rows, h]), rdq[0], 5e-2, 5e-2)
     if not w.backward:
         return
@@ -77,12 +77,19 @@ def test_full_size_sampled_parity(cuda_device, name):
     do = f64(x["do"][0, :, qh])
     k = f64(x["k"][0, :, g:g + 1])
     v = f64(x["v"][0, :, g:g + 1])
-    sk, sv = attention.attention_backward_keys(q, k, v, do, keys, kv_head=0)
+    sk, sv = attention.attention_backward_keys(q, k, v, do, keys, kv_head=0, d_from_bf16_o=True)
     assert_close("dK keys", f64(dk[0, keys, g]), sk, 5e-2, 5e-2)
     assert_close("dV keys", f64(dv[0, keys, g]), sv, 5e-2, 5e-2)
-    # invariants over every key
+    # Invariants over every key.  The stored bf16 values each carry a rounding
+    # error of at most half a bf16 spacing (<= 2^-8 |x|), independent across
+    # keys, so a sum over S keys is off by about sigma = 2^-7 / sqrt(12) *
+    # sqrt(sum x^2); the bound is 6 sigma plus 1e-3 relative.
+    def noise(t):
+        return 6.0 * 2.0 ** -7 / np.sqrt(12.0) * np.sqrt((t[0].double() ** 2).sum(dim=0).cpu().numpy())
     dk_sum = dk[0].double().sum(dim=0).cpu().numpy()
-    scale = float(np.abs(dk[0].double().cpu().numpy()).sum(axis=0).max())
-    assert np.abs(dk_sum).max() < 2e-3 * scale + 1.0
+    assert np.all(np.abs(dk_sum) <= noise(dk) + 1e-3), np.abs(dk_sum).max()
     do_grp = x["do"][0].double().reshape(w.seqlen, w.hkv, G, w.head_dim).sum(dim=(0, 2)).cpu().numpy()
-    assert_close("sum dV", dv[0].double().sum(dim=0).cpu().numpy(), do_grp, 2.0, 1e-2)
+    dv_sum = dv[0].double().sum(dim=0).cpu().numpy()
+    err = np.abs(dv_sum - do_grp)
+    bound = noise(dv) + 1e-3 * np.abs(do_grp)
+    assert np.all(err <= bound), (err.max(), float((err / bound).max()))

@@ -171,3 +171,23 @@ def test_sampled_rows_match_full():
     sk, sv = attention.attention_backward_keys(q, k, v, do, keys, kv_head=1)
     np.testing.assert_allclose(sk, dk[keys, 1], atol=1e-12)
     np.testing.assert_allclose(sv, dv[keys, 1], atol=1e-12)
+
+
+def test_round_bf16_matches_torch_conversion():
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal(100000) * 10.0 ** rng.integers(-6, 6, 100000),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.01171875, 65504.0, -3.5e-30]])
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(attention.round_bf16(x), want)
+
+
+def test_d_from_bf16_o_only_moves_the_d_term():
+    rng = np.random.default_rng(22)
+    q, k, v, do = _rand(rng, 16, 4, 2, 8)
+    exact = attention.attention_backward(q, k, v, do)
+    rounded = attention.attention_backward(q, k, v, do, d_from_bf16_o=True)
+    np.testing.assert_array_equal(exact[2], rounded[2])              # dV has no D term
+    o = exact[3]
+    np.testing.assert_allclose(rounded[5], np.einsum("shd,shd->hs", do, attention.round_bf16(o)),
+                               atol=1e-15)
+    assert 0 < np.abs(rounded[0] - exact[0]).max() < 1e-2
