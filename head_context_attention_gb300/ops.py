@@ -26,8 +26,9 @@ MODE_STEPWISE, MODE_FUSED = 0, 1
 
 EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loong_attn_check",
            "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_bwd",
-           "loong_lse_merge", "loong_headctx_pack", "loong_set_timing_events",
-           "loong_get_device_status")
+           "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack",
+           "loong_set_timing_events", "loong_get_device_status")
+NOALLOC_SCRATCH_BYTES = 32 << 20   # LOONG_NOALLOC_SCRATCH_BYTES
 
 
 class LoongAttnDesc(ctypes.Structure):
@@ -71,6 +72,7 @@ def lib():
         L.loong_ring_schedule.argtypes = [I32, I32, ctypes.POINTER(ctypes.c_int32)]
         L.loong_attn_fwd.argtypes = [D, P, P, P, P, P, P, SZ, P]
         L.loong_attn_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.loong_attn_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P]
         L.loong_lse_merge.argtypes = [I64, I32, I32, P, P, P, P, ctypes.c_int, P]
         L.loong_headctx_pack.argtypes = [I64, I32, I32, I64, I32, I32, ctypes.c_int, ctypes.c_int,
                                          P, P, P]

@@ -164,6 +164,36 @@ LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const v
                    loong_stream_t stream);
 
 /*
+ * Largest workspace, in bytes, that loong_attn_bwd_noalloc can serve: 32 MiB,
+ * e.g. S = 8192 tokens x 8 query heads x d = 128 in FUSED mode.
+ */
+#define LOONG_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * loong_attn_bwd without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin inside a framework that owns the whole
+ * device pool and hands it only inputs and outputs, or a latency-critical loop
+ * that cannot take cudaMalloc's implicit device synchronisation.  The paper
+ * has no counterpart; this is an interface convenience.
+ *   Same arguments, layouts and results as loong_attn_bwd, minus ws/ws_bytes.
+ *   Scratch lives in one static device array of LOONG_NOALLOC_SCRATCH_BYTES
+ *   that every GPU loading the library holds until the process exits.  The
+ *   call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *   routine.  Returns LOONG_ERR_WORKSPACE when
+ *   loong_attn_workspace_size(desc, 1) exceeds LOONG_NOALLOC_SCRATCH_BYTES.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one array and it keeps the last call's
+ *   contents (the parts that must start at zero are cleared by each call):
+ *   calls whose work overlaps on the GPU (other streams, other host threads)
+ *   race on it and must be serialised by the caller.
+ */
+LOONG_API int loong_attn_bwd_noalloc(const loong_attn_desc* desc, const void* q, const void* k,
+                                     const void* v, const void* o, const float* lse, const void* dout,
+                                     void* dq, void* dk, void* dv, loong_stream_t stream);
+
+/*
  * n-way log-sum-exp merge of partial attention results over disjoint key sets
  * (the pages leave the merge implicit; it is the rule under which softmax over
  * a union of key sets is recovered from the parts):
