@@ -190,9 +190,7 @@ size_t loong_attn_workspace_size(const loong_attn_desc* d, int pass) {
   if (pass == 0) return d->mode == LOONG_MODE_STEPWISE ? up(q_elems * 4) : 0;
   if (pass != 1) return 0;
   const size_t stats = 2 * static_cast<size_t>(d->batch) * d->hq * stat_row_len(ring_geom(*d));
-  size_t n = up(q_elems * 4) + up(stats * 4);
-  if (d->mode == LOONG_MODE_STEPWISE) n += 2 * up(kv_elems * 4);
-  return n;
+  return up(q_elems * 4) + up(stats * 4) + 2 * up(kv_elems * 4);
 }
 
 int loong_ring_schedule(int32_t inner, int32_t outer, int32_t* src) {
@@ -245,12 +243,8 @@ int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* dq_acc = reinterpret_cast<float*>(w);
   float* dvec = reinterpret_cast<float*>(w + up(q_elems * 4));
-  float* dk_acc = nullptr;
-  float* dv_acc = nullptr;
-  if (d->mode == LOONG_MODE_STEPWISE) {
-    dk_acc = reinterpret_cast<float*>(w + up(q_elems * 4) + up(stats * 4));
-    dv_acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dk_acc) + up(kv_elems * 4));
-  }
+  float* dk_acc = reinterpret_cast<float*>(w + up(q_elems * 4) + up(stats * 4));
+  float* dv_acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dk_acc) + up(kv_elems * 4));
   return launch_bwd(*d, q, k, v, o, lse, dout, dq, dk, dv, dq_acc, dvec, dk_acc, dv_acc, stream);
 }
 

@@ -10,10 +10,14 @@
 //   P^T  = exp2(S^T*scale*log2e - LSE*log2e),  dS^T = P^T * (dP^T - D)
 //   dV  += P^T dO                (P^T from tensor memory)
 //   dK  += dS^T Q                (dS^T from shared memory, K-major)
-//   dQ   = dS K  -> fp32 atomics into the dQ accumulator (dS^T read MN-major)
-// dK and dV stay in tensor memory for the whole walk and are written once
-// (FUSED) or added into fp32 accumulators (STEPWISE, one launch per step; a
-// step maps ranks to sources one to one, so no two CTAs share a tile).
+//   dQ   = dS K  -> fp32 atomics into the dQ accumulator; for d = 128 formed
+//                   as dQ^T = K^T dS^T so that a warp's atomics are coalesced
+// dK and dV stay in tensor memory and are folded into fp32 accumulators every
+// kFlush iterations; the last partial is added and written as bf16 (FUSED) or
+// left in the accumulators (STEPWISE, one launch per step; a step maps ranks to
+// sources one to one, so no two CTAs share a tile).  The compute warps form P^T
+// as soon as S^T is ready, while dP^T is still on the tensor cores, and drain
+// dQ while dK is computed.
 //
 // Warp roles (320 threads): warps 0-3 and 4-7 form two groups that each cover
 // all 128 TMEM lanes; group w handles query columns [64w, 64w+64) of S^T/dP^T
@@ -41,12 +45,20 @@ struct BwdCfg {
   static constexpr int ATOM_BYTES = kTile * 128;  // 16 KB
   static constexpr int TILE_BYTES = kTile * D * 2;
   static constexpr int DS_BYTES = kTile * kTile * 2;  // dS^T tile, bf16 [keys][queries]
-  static constexpr int NBARS = 1 + 2 * NS + 6;
+  static constexpr int NBARS = 1 + 2 * NS + 11;
   static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NBARS * 8 + 1024;
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t R0 = 0, R1 = 128, RV = 256, RK = 256 + D;
+  // dQ is formed transposed (head-dim on TMEM lanes) when d fills all 128 lanes:
+  // a warp's fp32 reductions for one query then cover 32 consecutive floats.
+  static constexpr bool DQ_T = D == 128;
 };
+
+// dK and dV build up in tensor memory; every kFlush iterations they are added
+// into fp32 accumulators in global memory and the tensor-memory sums restart,
+// which bounds the length of each tensor-core accumulation chain.
+constexpr int kFlush = 512;
 
 struct BwdArgs {
   int batch, S, hq, hkv, G;
@@ -60,7 +72,7 @@ struct BwdArgs {
   float* dq_acc;      // [B, S, Hq, D] fp32
   __nv_bfloat16* dk;  // FUSED outputs
   __nv_bfloat16* dv;
-  float* dk_acc;      // STEPWISE accumulators
+  float* dk_acc;      // fp32 accumulators [B, S, Hkv, D] (zeroed by the launcher)
   float* dv_acc;
   unsigned* err;
 };
@@ -88,11 +100,15 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NS;
-  uint64_t* sd_full = q_empty + C::NS;
-  uint64_t* pd_full = sd_full + 1;
-  uint64_t* dq_full = pd_full + 1;
-  uint64_t* dq_empty = dq_full + 1;
-  uint64_t* done_bar = dq_empty + 1;
+  uint64_t* s_full = q_empty + C::NS;   // S^T(i) in R0          (MMA -> warps)
+  uint64_t* dp_full = s_full + 1;       // dP^T(i) in R1         (MMA -> warps)
+  uint64_t* p_full = dp_full + 1;       // P^T(i) in R0          (warps -> MMA)
+  uint64_t* ds_full = p_full + 1;       // dS^T(i) in smem       (warps -> MMA)
+  uint64_t* dq_full = ds_full + 1;      // dQ(i) in R1           (MMA -> warps)
+  uint64_t* dq_empty = dq_full + 1;     // R1 drained            (warps -> MMA)
+  uint64_t* acc_full = dq_empty + 1;    // dK/dV ready to flush  (MMA -> warps)
+  uint64_t* acc_empty = acc_full + 1;   // dK/dV flushed         (warps -> MMA)
+  uint64_t* done_bar = acc_empty + 1;
   uint64_t* drain = done_bar + 1;
   volatile int* abort_flag = &abort_sh;
 
@@ -110,9 +126,10 @@ __global__ void __launch_bounds__(320, 1)
   const int klen = min(kTile, (bk + 1) * g.blk - k0);
 
   QWalk walk;
-  walk.init(g, a.G, bk, kt, a.t_begin, a.t_end);
+  walk.init(g, a.G, bk, kt, a.t_begin, a.t_end, kt);
   const int n = walk.count();
   if (n == 0) return;
+  const int nflush = (n - 1) / kFlush;  // flushes before the final write
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -123,10 +140,14 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    mbar_init(sd_full, 1);
-    mbar_init(pd_full, 8);
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 8);
+    mbar_init(ds_full, 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 8);
     mbar_init(done_bar, 1);
     mbar_init(drain, 1);
     abort_sh = 0;
@@ -181,7 +202,8 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
       constexpr uint32_t id_dkv = idesc_bf16(128, D, false, true);   // dV, dK: B MN-major
-      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // dQ: A and B MN-major
+      constexpr uint32_t id_dq = C::DQ_T ? idesc_bf16(128, 128, true, true)  // dQ^T: d x queries
+                                         : idesc_bf16(128, D, true, true);   // dQ: queries x d
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
                      o_addr = smem_u32(sdO), ds_addr = smem_u32(sdS);
       // X^T[keys x queries] = A[keys x d] * B[queries x d]^T, both K-major
@@ -197,42 +219,65 @@ __global__ void __launch_bounds__(320, 1)
       if (ok) {
         tc_fence_after();
         mm_s(C::R0, k_addr, q_addr);
+        mma_commit(s_full);
         mm_s(C::R1, v_addr, o_addr);
-        mma_commit(sd_full);
+        mma_commit(dp_full);
+        bool fresh = true;  // next dV / dK start a new tensor-memory sum
         for (int i = 0; i < n; ++i) {
           const int s = i % C::NS;
-          if (!mbar_wait(pd_full, i & 1, abort_flag, a.err)) break;
-          tc_fence_after();
           const uint32_t qs = q_addr + s * C::TILE_BYTES, os = o_addr + s * C::TILE_BYTES;
+          if (!mbar_wait(p_full, i & 1, abort_flag, a.err)) break;
+          tc_fence_after();
           // dV += P^T dO: A = P^T (TMEM, 8 columns per 16 queries; queries 64..127
           // start at column 64), B = dO MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_ts(tbase + C::RV, tbase + C::R0 + (kk >> 2) * 64 + (kk & 3) * 8,
-                   sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, i > 0 || kk > 0);
+                   sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, !fresh || kk > 0);
+          if (!mbar_wait(ds_full, i & 1, abort_flag, a.err)) break;
+          tc_fence_after();
+          // First, so that the drain of dQ overlaps the dK product:
+          //   D = 128: dQ^T = K^T dS^T, A = K read MN-major (head-dim on TMEM lanes),
+          //            B = dS^T MN-major (queries on columns);
+          //   D = 64:  dQ = dS K, A = dS^T read MN-major, B = K MN-major.
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint64_t kd = sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024);
+            const uint64_t sd = sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024);
+            if constexpr (C::DQ_T)
+              mma_ss(tbase + C::R1, kd, sd, id_dq, kk > 0);
+            else
+              mma_ss(tbase + C::R1, sd, kd, id_dq, kk > 0);
+          }
+          mma_commit(dq_full);
           // dK += dS^T Q: A = dS^T K-major (queries contiguous), B = Q MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
             mma_ss(tbase + C::RK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::ATOM_BYTES, 1024),
-                   id_dkv, i > 0 || kk > 0);
+                   id_dkv, !fresh || kk > 0);
           }
-          // dQ = dS K: A = dS (dS^T read MN-major), B = K MN-major
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tbase + C::R1, sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024),
-                   sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024), id_dq, kk > 0);
-          mma_commit(dq_full);
           mma_commit(&q_empty[s]);
+          fresh = false;
+          const bool flush = i + 1 < n && (i + 1) % kFlush == 0;
+          if (flush) {
+            mma_commit(acc_full);
+            fresh = true;
+          }
           if (i + 1 < n) {
             const int s1 = (i + 1) % C::NS;
             if (!mbar_wait(&q_full[s1], ((i + 1) / C::NS) & 1, abort_flag, a.err)) break;
             tc_fence_after();
-            mm_s(C::R0, k_addr, q_addr + s1 * C::TILE_BYTES);
+            mm_s(C::R0, k_addr, q_addr + s1 * C::TILE_BYTES);  // R0's P^T was read by dV(i), issued earlier
+            mma_commit(s_full);
             if (!mbar_wait(dq_empty, i & 1, abort_flag, a.err)) break;
             tc_fence_after();
             mm_s(C::R1, v_addr, o_addr + s1 * C::TILE_BYTES);
-            mma_commit(sd_full);
+            mma_commit(dp_full);
+            if (flush) {
+              if (!mbar_wait(acc_empty, ((i + 1) / kFlush - 1) & 1, abort_flag, a.err)) break;
+              tc_fence_after();
+            }
           }
         }
         mma_commit(done_bar);
@@ -247,13 +292,16 @@ __global__ void __launch_bounds__(320, 1)
     const int row = quarter * 32 + lane;  // key row in the pass, query row in the dQ drain
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const bool key_ok = row < klen;
+    const int64_t krow = (row_base + k0 + row) * a.hkv + kvh;
+    // group 0 owns dV, group 1 owns dK (keys on lanes)
+    const uint32_t acc_col = grp == 0 ? C::RV : C::RK;
+    float* acc_glob = (grp == 0 ? a.dv_acc : a.dk_acc) + krow * D;
+    const float acc_mul = grp == 0 ? 1.f : a.scale;
     bool ok = true;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
+    };
     for (int i = 0; i < n; ++i, walk.advance()) {
-      if (!__all_sync(0xffffffffu, mbar_wait(sd_full, i & 1, abort_flag, a.err))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
       const int head = kvh * a.G + walk.head;
       const int q0 = walk.q0();
       const int qlen = walk.qlen();
@@ -261,38 +309,36 @@ __global__ void __launch_bounds__(320, 1)
       const float* lse_row = a.lse2 + (static_cast<int64_t>(b) * a.hq + head) * a.stat_len;
       const float* d_row = a.dstat + (static_cast<int64_t>(b) * a.hq + head) * a.stat_len;
       const int qidx = walk.bq * a.blk_pad + walk.qi * kTile;
-      // Two 32-column chunks of this group's 64 queries.
-#pragma unroll 1
+      // ---- P^T = exp2(S^T * scale * log2e - LSE * log2e), two 32-query chunks
+      if (!warp_wait(s_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float pv[2][32];
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int cbase = grp * 64 + ch * 32;  // first query column of the chunk
-        uint32_t sv[32], dpv[32];
+        uint32_t sv[32];
         tmem_ld32(tbase + t_lane + C::R0 + cbase, sv);
-        tmem_ld32(tbase + t_lane + C::R1 + cbase, dpv);
         tmem_wait_ld();
         uint32_t pk[16];
-        uint32_t dsk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           // the same query indices in every lane: broadcast loads of the
           // padded per-block row statistics (aligned, always in bounds)
           const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_row + qidx + cbase + e));
-          const float4 d4 = __ldg(reinterpret_cast<const float4*>(d_row + qidx + cbase + e));
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int c = cbase + e + u;
             const bool live = key_ok && c < qlen && (!dg || row <= c);
-            // masked columns may hold statistics of other rows or padding: select, never multiply
+            // masked columns may hold statistics of other rows or padding: select
             const float x = fast_exp2(fmaf(__uint_as_float(sv[e + u]), a.scale_log2, -lv[u]));
-            p[u] = live ? x : 0.f;
-            ds[u] = live ? x * (__uint_as_float(dpv[e + u]) - dv4[u]) : 0.f;
+            pv[ch][e + u] = live ? x : 0.f;
           }
-          pk[e / 2] = pack_bf16(p[0], p[1]);
-          pk[e / 2 + 1] = pack_bf16(p[2], p[3]);
-          dsk[e / 2] = pack_bf16(ds[0], ds[1]);
-          dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+          pk[e / 2] = pack_bf16(pv[ch][e], pv[ch][e + 1]);
+          pk[e / 2 + 1] = pack_bf16(pv[ch][e + 2], pv[ch][e + 3]);
         }
         // P^T (bf16 pairs) into this group's own half of R0, columns
         // [64 grp + 16 ch, +16): already read by this group, never read by the other.
@@ -302,6 +348,39 @@ __global__ void __launch_bounds__(320, 1)
             "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]),
             "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
             : "memory");
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+
+      // ---- dS^T = P^T * (dP^T - D) into shared memory
+      if (!warp_wait(dp_full, i & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int cbase = grp * 64 + ch * 32;
+        uint32_t dpv[32];
+        tmem_ld32(tbase + t_lane + C::R1 + cbase, dpv);
+        tmem_wait_ld();
+        uint32_t dsk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 d4 = __ldg(reinterpret_cast<const float4*>(d_row + qidx + cbase + e));
+          const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            // pv is 0 on masked columns; D may be another row's or padding there
+            const float p = pv[ch][e + u];
+            ds[u] = p != 0.f ? p * (__uint_as_float(dpv[e + u]) - dv4[u]) : 0.f;
+          }
+          dsk[e / 2] = pack_bf16(ds[0], ds[1]);
+          dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+        }
         // dS^T row `row`, queries [cbase, cbase+32): 4 of the 8 16-byte units of
         // this group's 128-byte line in atom `grp`, 128-byte swizzled.
         uint8_t* line = sdS + grp * C::ATOM_BYTES + row * 128;
@@ -316,19 +395,32 @@ __global__ void __launch_bounds__(320, 1)
           *reinterpret_cast<uint4*>(line + ((unit ^ (row & 7)) << 4)) = w;
         }
       }
-      tmem_wait_st();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(pd_full);
+      if (lane == 0) mbar_arrive(ds_full);
 
       // ---- drain dQ (queries on lanes) into the fp32 accumulator
-      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, i & 1, abort_flag, a.err))) {
+      if (!warp_wait(dq_full, i & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      {
+      if constexpr (C::DQ_T) {
+        // lanes = head-dim index `row`, columns = queries [64 grp, 64 grp + 64)
+        float* dst = a.dq_acc + ((row_base + q0) * a.hq + head) * D + row;
+        const int64_t qstride = static_cast<int64_t>(a.hq) * D;
+#pragma unroll 1
+        for (int cb = 0; cb < 2; ++cb) {
+          uint32_t qv[32];
+          const int c0 = grp * 64 + cb * 32;
+          tmem_ld32(tbase + t_lane + C::R1 + c0, qv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c0 + e < qlen) atomicAdd(dst + (c0 + e) * qstride, __uint_as_float(qv[e]) * a.scale);
+        }
+      } else {
         const bool q_ok = row < qlen;
         float* dst = a.dq_acc + ((row_base + q0 + row) * a.hq + head) * D + grp * (D / 2);
 #pragma unroll 1
@@ -350,43 +442,79 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
+
+      // ---- every kFlush iterations: fold dV / dK into the fp32 accumulators
+      if (i + 1 < n && (i + 1) % kFlush == 0) {
+        if (!warp_wait(acc_full, ((i + 1) / kFlush - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(tbase + t_lane + acc_col + cb * 32, v);
+          tmem_wait_ld();
+          if (key_ok) {
+            float4* dst = reinterpret_cast<float4*>(acc_glob + cb * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              float4 x = dst[v4];
+              x.x += __uint_as_float(v[v4 * 4 + 0]) * acc_mul;
+              x.y += __uint_as_float(v[v4 * 4 + 1]) * acc_mul;
+              x.z += __uint_as_float(v[v4 * 4 + 2]) * acc_mul;
+              x.w += __uint_as_float(v[v4 * 4 + 3]) * acc_mul;
+              dst[v4] = x;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+      }
     }
     // ---------------------------------------------------------- epilogue
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(done_bar, 0, abort_flag, a.err));
+    if (ok) ok = warp_wait(done_bar, 0);
     if (ok) {
       tc_fence_after();
-      // group 0 writes dV, group 1 writes dK (keys on lanes)
-      const uint32_t src = grp == 0 ? C::RV : C::RK;
-      const float mul = grp == 0 ? 1.f : a.scale;
-      const int64_t krow = (row_base + k0 + row) * a.hkv + kvh;
+      // the accumulator holds earlier flushes (FUSED) or earlier steps (STEPWISE)
+      const bool add_glob = STEP || nflush > 0;
 #pragma unroll 1
       for (int cb = 0; cb < D / 32; ++cb) {
         uint32_t v[32];
-        tmem_ld32(tbase + t_lane + src + cb * 32, v);
+        tmem_ld32(tbase + t_lane + acc_col + cb * 32, v);
         tmem_wait_ld();
         if (key_ok) {
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(v[e]) * acc_mul;
+          if (add_glob) {
+            const float4* src = reinterpret_cast<const float4*>(acc_glob + cb * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4) {
+              const float4 y = src[v4];
+              x[v4 * 4 + 0] += y.x;
+              x[v4 * 4 + 1] += y.y;
+              x[v4 * 4 + 2] += y.z;
+              x[v4 * 4 + 3] += y.w;
+            }
+          }
           if constexpr (!STEP) {
             __nv_bfloat16* dst = (grp == 0 ? a.dv : a.dk) + krow * D + cb * 32;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 w;
-              w.x = pack_bf16(__uint_as_float(v[v4 * 8 + 0]) * mul, __uint_as_float(v[v4 * 8 + 1]) * mul);
-              w.y = pack_bf16(__uint_as_float(v[v4 * 8 + 2]) * mul, __uint_as_float(v[v4 * 8 + 3]) * mul);
-              w.z = pack_bf16(__uint_as_float(v[v4 * 8 + 4]) * mul, __uint_as_float(v[v4 * 8 + 5]) * mul);
-              w.w = pack_bf16(__uint_as_float(v[v4 * 8 + 6]) * mul, __uint_as_float(v[v4 * 8 + 7]) * mul);
+              w.x = pack_bf16(x[v4 * 8 + 0], x[v4 * 8 + 1]);
+              w.y = pack_bf16(x[v4 * 8 + 2], x[v4 * 8 + 3]);
+              w.z = pack_bf16(x[v4 * 8 + 4], x[v4 * 8 + 5]);
+              w.w = pack_bf16(x[v4 * 8 + 6], x[v4 * 8 + 7]);
               reinterpret_cast<uint4*>(dst)[v4] = w;
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>((grp == 0 ? a.dv_acc : a.dk_acc) + krow * D + cb * 32);
+            float4* dst = reinterpret_cast<float4*>(acc_glob + cb * 32);
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-              float4 x = dst[v4];
-              x.x += __uint_as_float(v[v4 * 4 + 0]) * mul;
-              x.y += __uint_as_float(v[v4 * 4 + 1]) * mul;
-              x.z += __uint_as_float(v[v4 * 4 + 2]) * mul;
-              x.w += __uint_as_float(v[v4 * 4 + 3]) * mul;
-              dst[v4] = x;
-            }
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(x[v4 * 4], x[v4 * 4 + 1], x[v4 * 4 + 2], x[v4 * 4 + 3]);
           }
         }
       }
@@ -469,11 +597,9 @@ int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const voi
   int st;
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (step) {
-    if ((e = cudaMemsetAsync(dk_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(dv_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess)
-      return cuda_fail(e);
-  }
+  if ((e = cudaMemsetAsync(dk_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess ||
+      (e = cudaMemsetAsync(dv_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess)
+    return cuda_fail(e);
   if ((st = launch_bwd_rowstats(d, o, dout, lse, dvec, stream)) != LOONG_OK) return st;
   if (d.head_dim == 128)
     st = step ? launch_bwd_t<128, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream)

@@ -116,12 +116,18 @@ __host__ __device__ inline int ring_dst(int j, int t, int inner, int outer) {
 }
 
 // The (query tile, head) pairs that meet key tile (block bk, tile kt) over
-// ring steps [t0, t1), in the order the K/V chunk visits ranks.
+// ring steps [t0, t1), in the order the K/V chunk visits ranks: step by step,
+// the destination rank's block A then B, then its query tiles and the G heads
+// of the kv group.  Within a block the tiles (and the heads) start at an offset
+// `rot`, so that CTAs of neighbouring key tiles, which walk the same blocks at
+// the same time, add into different dQ rows.
 struct QWalk {
   RingGeom g;
-  int G, bk, kt, j, t, t1, part, qi, qi_end, head, bq;
+  int G, bk, kt, j, t, t1, part, rot;
+  int qlo, len, k, hk;  // tiles [qlo, ntile) of the current block; position k; head position hk
+  int qi, head, bq;
 
-  __host__ __device__ void init(const RingGeom& geom, int G_, int bk_, int kt_, int t0, int t1_) {
+  __host__ __device__ void init(const RingGeom& geom, int G_, int bk_, int kt_, int t0, int t1_, int rot_ = 0) {
     g = geom;
     G = G_;
     bk = bk_;
@@ -130,38 +136,48 @@ struct QWalk {
     t = t0;
     t1 = t1_;
     part = 0;
-    qi = -1;
-    head = 0;
-    next_block();
+    rot = rot_ < 0 ? 0 : rot_;
+    next_block(true);
   }
-  // Position on the first query tile of the next block that sees bk.
-  __host__ __device__ void next_block() {
+  // Settle on the first (tile, head) of the current or next block that sees bk.
+  __host__ __device__ void next_block(bool same) {
+    if (!same) step_part();
     while (t < t1) {
-      if (qi < 0) {
-        const int c = ring_dst(j, t, g.inner, g.outer);
-        bq = rank_block(g, c, part);
-        qi_end = g.ntile;
-        qi = bk < bq ? 0 : (bk == bq ? kt : g.ntile);
-        if (qi < qi_end) return;
+      const int c = ring_dst(j, t, g.inner, g.outer);
+      bq = rank_block(g, c, part);
+      qlo = bk < bq ? 0 : (bk == bq ? kt : g.ntile);
+      len = g.ntile - qlo;
+      if (len > 0) {
+        k = 0;
+        hk = 0;
+        set();
+        return;
       }
-      qi = -1;
-      if (++part == rank_parts(g)) {
-        part = 0;
-        ++t;
-      }
+      step_part();
     }
   }
-  __host__ __device__ bool done() const { return t >= t1; }
-  __host__ __device__ void advance() {
-    if (++head < G) return;
-    head = 0;
-    if (++qi < qi_end) return;
-    qi = -1;
+  __host__ __device__ void step_part() {
     if (++part == rank_parts(g)) {
       part = 0;
       ++t;
     }
-    next_block();
+  }
+  __host__ __device__ void set() {
+    qi = qlo + (k + rot) % len;
+    head = (hk + rot) % G;
+  }
+  __host__ __device__ bool done() const { return t >= t1; }
+  __host__ __device__ void advance() {
+    if (++hk < G) {
+      set();
+      return;
+    }
+    hk = 0;
+    if (++k < len) {
+      set();
+      return;
+    }
+    next_block(false);
   }
   __host__ __device__ int q0() const { return bq * g.blk + qi * kTile; }
   __host__ __device__ int qlen() const {

@@ -117,8 +117,8 @@ LOONG_API int loong_attn_check(const loong_attn_desc* desc);
  *   fwd, FUSED: 0.  fwd, STEPWISE: fp32 O accumulator [B,S,Hq,d].
  *   bwd: fp32 dQ accumulator [B,S,Hq,d] + fp32 row statistics (LSE*log2 e
  *        and D = rowsum(dO*O)), 2 x B x Hq x (nblocks*roundup(blk,4) + 128)
- *        values, with nblocks = 2cp (ZIGZAG) or cp and blk = S/nblocks;
- *        STEPWISE adds fp32 dK, dV accumulators [B,S,Hkv,d] each.
+ *        values, with nblocks = 2cp (ZIGZAG) or cp and blk = S/nblocks,
+ *        + fp32 dK, dV accumulators [B,S,Hkv,d] each.
  *   Each part starts on a 256-byte boundary.
  */
 LOONG_API size_t loong_attn_workspace_size(const loong_attn_desc* desc, int pass);

@@ -86,7 +86,7 @@ def test_workspace_sizes(loong_lib):
     blk = w.seqlen // (2 * w.cp)
     stats = 2 * w.hq * (2 * w.cp * ((blk + 3) // 4 * 4) + 128) * 4
     up = lambda x: (x + 255) // 256 * 256
-    assert ops.loong_attn_workspace_size(fused, 1) == up(q_el * 4) + up(stats)
+    assert ops.loong_attn_workspace_size(fused, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
     assert ops.loong_attn_workspace_size(step, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
     bad = _desc(hq=30)
     assert ops.loong_attn_workspace_size(bad, 0) == 0
