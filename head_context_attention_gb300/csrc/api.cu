@@ -127,6 +127,27 @@ int make_head_tile_map(CUtensorMap* map, const void* base, int64_t rows, int hea
   return LOONG_OK;
 }
 
+int make_f32_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (!enc) return LOONG_ERR_CUDA;
+  if (!aligned16(base)) return LOONG_ERR_INVALID_ARG;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(d) * 4 * static_cast<cuuint64_t>(heads)};
+  const cuuint32_t box[3] = {32, 1, 128};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed (%d)",
+                  static_cast<int>(r));
+    return LOONG_ERR_CUDA;
+  }
+  return LOONG_OK;
+}
+
 RingGeom ring_geom(const loong_attn_desc& d) {
   RingGeom g;
   g.cp = d.cp;

@@ -10,8 +10,8 @@
 //   P^T  = exp2(S^T*scale*log2e - LSE*log2e),  dS^T = P^T * (dP^T - D)
 //   dV  += P^T dO                (P^T from tensor memory)
 //   dK  += dS^T Q                (dS^T from shared memory, K-major)
-//   dQ   = dS K  -> fp32 atomics into the dQ accumulator; for d = 128 formed
-//                   as dQ^T = K^T dS^T so that a warp's atomics are coalesced
+//   dQ   = dS K  -> staged in shared memory, added into the fp32 dQ
+//                   accumulator by TMA bulk tensor reductions
 // dK and dV stay in tensor memory and are folded into fp32 accumulators every
 // kFlush iterations; the last partial is added and written as bf16 (FUSED) or
 // left in the accumulators (STEPWISE, one launch per step; a step maps ranks to
@@ -45,14 +45,19 @@ struct BwdCfg {
   static constexpr int ATOM_BYTES = kTile * 128;  // 16 KB
   static constexpr int TILE_BYTES = kTile * D * 2;
   static constexpr int DS_BYTES = kTile * kTile * 2;  // dS^T tile, bf16 [keys][queries]
-  static constexpr int NBARS = 1 + 2 * NS + 11;
-  static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NBARS * 8 + 1024;
+  static constexpr int NBARS = 1 + 2 * NS + 14;
+  static constexpr int STAT_BYTES = 2 * kTile * 4;  // LSE*log2e and D of one query tile
+  // Tiles first (1024-byte aligned, checked at run time), then the row
+  // statistics stages, the barriers, the TMEM base address and the abort flag.
+  static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16;
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t R0 = 0, R1 = 128, RV = 256, RK = 256 + D;
-  // dQ is formed transposed (head-dim on TMEM lanes) when d fills all 128 lanes:
-  // a warp's fp32 reductions for one query then cover 32 consecutive floats.
-  static constexpr bool DQ_T = D == 128;
+  // dQ leaves through TMA bulk reductions of 32-float x 128-row boxes; the
+  // boxes are staged in the Q / dO stage of the iteration they belong to.
+  static constexpr int DQ_BOXES = D / 32;
+  static constexpr int BOX_BYTES = kTile * 128;
+  static constexpr int BOXES_PER_STAGE = TILE_BYTES / BOX_BYTES;
 };
 
 // dK and dV build up in tensor memory; every kFlush iterations they are added
@@ -83,20 +88,20 @@ template <int D, bool STEP>
 __global__ void __launch_bounds__(320, 1)
     ring_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                    const BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
   using C = BwdCfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_sh;
-
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // uniform over the CTA; the swizzled tiles need it
+    if (threadIdx.x == 0) atomicOr(a.err, kErrSmemAlign);
+    return;
+  }
   uint8_t* sK = smem;
   uint8_t* sV = sK + C::TILE_BYTES;
   uint8_t* sQ = sV + C::TILE_BYTES;              // NS stages
   uint8_t* sdO = sQ + C::NS * C::TILE_BYTES;     // NS stages
   uint8_t* sdS = sdO + C::NS * C::TILE_BYTES;    // [2 query atoms][128 keys][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sdS + C::DS_BYTES);
+  float* sStat = reinterpret_cast<float*>(sdS + C::DS_BYTES);  // NS x [LSE2[128], D[128]]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sStat) + C::NS * C::STAT_BYTES);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + C::NS;
@@ -106,10 +111,14 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* ds_full = p_full + 1;       // dS^T(i) in smem       (warps -> MMA)
   uint64_t* dq_full = ds_full + 1;      // dQ(i) in R1           (MMA -> warps)
   uint64_t* dq_empty = dq_full + 1;     // R1 drained            (warps -> MMA)
-  uint64_t* acc_full = dq_empty + 1;    // dK/dV ready to flush  (MMA -> warps)
+  uint64_t* dk_done = dq_empty + 1;     // dK(i) done: Q/dO stage free for staging
+  uint64_t* staged = dk_done + 1;       // [2] a group's dQ boxes are in smem (warps -> its issuer)
+  uint64_t* acc_full = staged + 2;      // dK/dV ready to flush  (MMA -> warps)
   uint64_t* acc_empty = acc_full + 1;   // dK/dV flushed         (warps -> MMA)
   uint64_t* done_bar = acc_empty + 1;
   uint64_t* drain = done_bar + 1;
+  uint32_t& tmem_base_sh = *reinterpret_cast<uint32_t*>(bars + C::NBARS);
+  int& abort_sh = *(reinterpret_cast<int*>(bars + C::NBARS) + 1);
   volatile int* abort_flag = &abort_sh;
 
   // ---- work item: (batch, kv head, key tile); early (heavy) key tiles first
@@ -126,7 +135,7 @@ __global__ void __launch_bounds__(320, 1)
   const int klen = min(kTile, (bk + 1) * g.blk - k0);
 
   QWalk walk;
-  walk.init(g, a.G, bk, kt, a.t_begin, a.t_end, kt);
+  walk.init(g, a.G, bk, kt, a.t_begin, a.t_end);
   const int n = walk.count();
   if (n == 0) return;
   const int nflush = (n - 1) / kFlush;  // flushes before the final write
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
+      mbar_init(&q_empty[s], 2);  // both compute groups, after their dQ boxes are read
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -146,6 +155,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(ds_full, 8);
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
+    mbar_init(dk_done, 1);
+    mbar_init(&staged[0], 4);
+    mbar_init(&staged[1], 4);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
     mbar_init(done_bar, 1);
@@ -162,6 +174,7 @@ __global__ void __launch_bounds__(320, 1)
     tma_prefetch_map(&tmK);
     tma_prefetch_map(&tmV);
     tma_prefetch_map(&tmO);
+    tma_prefetch_map(&tmDQ);
   }
   tc_fence_before();
   __syncthreads();
@@ -184,11 +197,16 @@ __global__ void __launch_bounds__(320, 1)
         if (i >= C::NS && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         const int head = kvh * a.G + walk.head;
         const int qrow = static_cast<int>(row_base + walk.q0());
-        mbar_expect_tx(&q_full[s], 2 * C::TILE_BYTES);
+        mbar_expect_tx(&q_full[s], 2 * C::TILE_BYTES + C::STAT_BYTES);
         for (int at = 0; at < C::ATOMS; ++at) {
           tma_load_3d(sQ + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, &q_full[s], at * 64, head, qrow);
           tma_load_3d(sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, head, qrow);
         }
+        // this tile's row statistics: 16-byte aligned and in bounds by construction
+        const int64_t srow = (static_cast<int64_t>(b) * a.hq + head) * a.stat_len + walk.bq * a.blk_pad +
+                             walk.qi * kTile;
+        bulk_load(sStat + s * (2 * kTile), a.lse2 + srow, kTile * 4, &q_full[s]);
+        bulk_load(sStat + s * (2 * kTile) + kTile, a.dstat + srow, kTile * 4, &q_full[s]);
         ++issued;
       }
       mbar_drain(kv_full, 0, a.err);
@@ -202,8 +220,7 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
       constexpr uint32_t id_dkv = idesc_bf16(128, D, false, true);   // dV, dK: B MN-major
-      constexpr uint32_t id_dq = C::DQ_T ? idesc_bf16(128, 128, true, true)  // dQ^T: d x queries
-                                         : idesc_bf16(128, D, true, true);   // dQ: queries x d
+      constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // dQ: A and B MN-major
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
                      o_addr = smem_u32(sdO), ds_addr = smem_u32(sdS);
       // X^T[keys x queries] = A[keys x d] * B[queries x d]^T, both K-major
@@ -236,19 +253,12 @@ __global__ void __launch_bounds__(320, 1)
                    sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, !fresh || kk > 0);
           if (!mbar_wait(ds_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
-          // First, so that the drain of dQ overlaps the dK product:
-          //   D = 128: dQ^T = K^T dS^T, A = K read MN-major (head-dim on TMEM lanes),
-          //            B = dS^T MN-major (queries on columns);
-          //   D = 64:  dQ = dS K, A = dS^T read MN-major, B = K MN-major.
+          // dQ = dS K: A = dS (dS^T read MN-major), B = K MN-major; first, so
+          // the drain of dQ overlaps the dK product
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t kd = sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024);
-            const uint64_t sd = sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024);
-            if constexpr (C::DQ_T)
-              mma_ss(tbase + C::R1, kd, sd, id_dq, kk > 0);
-            else
-              mma_ss(tbase + C::R1, sd, kd, id_dq, kk > 0);
-          }
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            mma_ss(tbase + C::R1, sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024),
+                   sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024), id_dq, kk > 0);
           mma_commit(dq_full);
           // dK += dS^T Q: A = dS^T K-major (queries contiguous), B = Q MN-major
 #pragma unroll
@@ -257,7 +267,7 @@ __global__ void __launch_bounds__(320, 1)
             mma_ss(tbase + C::RK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::ATOM_BYTES, 1024),
                    id_dkv, !fresh || kk > 0);
           }
-          mma_commit(&q_empty[s]);
+          mma_commit(dk_done);
           fresh = false;
           const bool flush = i + 1 < n && (i + 1) % kFlush == 0;
           if (flush) {
@@ -306,9 +316,9 @@ __global__ void __launch_bounds__(320, 1)
       const int q0 = walk.q0();
       const int qlen = walk.qlen();
       const bool dg = walk.diag();
-      const float* lse_row = a.lse2 + (static_cast<int64_t>(b) * a.hq + head) * a.stat_len;
-      const float* d_row = a.dstat + (static_cast<int64_t>(b) * a.hq + head) * a.stat_len;
-      const int qidx = walk.bq * a.blk_pad + walk.qi * kTile;
+      // row statistics of this tile, staged by the producer with Q and dO
+      const float* lse_row = sStat + (i % C::NS) * (2 * kTile);
+      const float* d_row = lse_row + kTile;
       // ---- P^T = exp2(S^T * scale * log2e - LSE * log2e), two 32-query chunks
       if (!warp_wait(s_full, i & 1)) {
         ok = false;
@@ -325,9 +335,8 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          // the same query indices in every lane: broadcast loads of the
-          // padded per-block row statistics (aligned, always in bounds)
-          const float4 l4 = __ldg(reinterpret_cast<const float4*>(lse_row + qidx + cbase + e));
+          // the same query indices in every lane: broadcast shared-memory reads
+          const float4 l4 = *reinterpret_cast<const float4*>(lse_row + cbase + e);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -369,7 +378,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t dsk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 d4 = __ldg(reinterpret_cast<const float4*>(d_row + qidx + cbase + e));
+          const float4 d4 = *reinterpret_cast<const float4*>(d_row + cbase + e);
           const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
           float ds[4];
 #pragma unroll
@@ -400,48 +409,64 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
 
-      // ---- drain dQ (queries on lanes) into the fp32 accumulator
+      // ---- drain dQ (queries on lanes): TMEM -> registers, R1 released, then
+      // staged (fp32, 128-byte swizzled boxes of 32 columns) into this
+      // iteration's Q / dO stage once dK(i) no longer reads it, and added into
+      // the fp32 accumulator by TMA bulk reductions.
       if (!warp_wait(dq_full, i & 1)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if constexpr (C::DQ_T) {
-        // lanes = head-dim index `row`, columns = queries [64 grp, 64 grp + 64)
-        float* dst = a.dq_acc + ((row_base + q0) * a.hq + head) * D + row;
-        const int64_t qstride = static_cast<int64_t>(a.hq) * D;
-#pragma unroll 1
-        for (int cb = 0; cb < 2; ++cb) {
-          uint32_t qv[32];
-          const int c0 = grp * 64 + cb * 32;
-          tmem_ld32(tbase + t_lane + C::R1 + c0, qv);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c0 + e < qlen) atomicAdd(dst + (c0 + e) * qstride, __uint_as_float(qv[e]) * a.scale);
-        }
-      } else {
+      {
         const bool q_ok = row < qlen;
-        float* dst = a.dq_acc + ((row_base + q0 + row) * a.hq + head) * D + grp * (D / 2);
-#pragma unroll 1
-        for (int cb = 0; cb < D / 64; ++cb) {
-          uint32_t qv[32];
-          tmem_ld32(tbase + t_lane + C::R1 + grp * (D / 2) + cb * 32, qv);
-          tmem_wait_ld();
-          if (q_ok) {
+        uint32_t qv[D / 64][32];
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4) {
-              float4 x = make_float4(__uint_as_float(qv[v4 * 4]) * a.scale, __uint_as_float(qv[v4 * 4 + 1]) * a.scale,
-                                     __uint_as_float(qv[v4 * 4 + 2]) * a.scale,
-                                     __uint_as_float(qv[v4 * 4 + 3]) * a.scale);
-              atomicAdd(reinterpret_cast<float4*>(dst + cb * 32) + v4, x);
-            }
+        for (int cb = 0; cb < D / 64; ++cb) tmem_ld32(tbase + t_lane + C::R1 + grp * (D / 2) + cb * 32, qv[cb]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_empty);
+        if (!warp_wait(dk_done, i & 1)) {
+          ok = false;
+          break;
+        }
+        const int s = i % C::NS;
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) {
+          const int box = grp * (D / 64) + cb;
+          uint8_t* base = box < C::BOXES_PER_STAGE ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
+                                                   : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
+          uint8_t* line = base + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (q_ok)
+              x = make_float4(__uint_as_float(qv[cb][c * 4]) * a.scale, __uint_as_float(qv[cb][c * 4 + 1]) * a.scale,
+                              __uint_as_float(qv[cb][c * 4 + 2]) * a.scale,
+                              __uint_as_float(qv[cb][c * 4 + 3]) * a.scale);
+            *reinterpret_cast<float4*>(line + ((c ^ (row & 7)) << 4)) = x;
           }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&staged[grp]);
+        // one thread per group issues the group's reductions once its four
+        // warps have staged (a bounded wait: never a plain barrier here)
+        if (quarter == 0 && lane == 0 && mbar_wait(&staged[grp], i & 1, abort_flag, a.err)) {
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb) {
+            const int box = grp * (D / 64) + cb;
+            const uint8_t* base = box < C::BOXES_PER_STAGE
+                                      ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
+                                      : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
+            tma_reduce_add_3d(&tmDQ, base, box * 32, head, static_cast<int>(row_base + q0));
+          }
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(&q_empty[s]);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
 
       // ---- every kFlush iterations: fold dV / dK into the fp32 accumulators
       if (i + 1 < n && (i + 1) % kFlush == 0) {
@@ -473,6 +498,8 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) mbar_arrive(acc_empty);
       }
     }
+    // the dQ reductions this thread issued must land before the kernel ends
+    if (quarter == 0 && lane == 0) bulk_wait_all();
     // ---------------------------------------------------------- epilogue
     if (ok) ok = warp_wait(done_bar, 0);
     if (ok) {
@@ -541,6 +568,8 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   if ((st = make_head_tile_map(&mk, k, rows, d.hkv, D)) != LOONG_OK) return st;
   if ((st = make_head_tile_map(&mv, v, rows, d.hkv, D)) != LOONG_OK) return st;
   if ((st = make_head_tile_map(&mo, dout, rows, d.hq, D)) != LOONG_OK) return st;
+  CUtensorMap mdq;
+  if ((st = make_f32_tile_map(&mdq, dq_acc, rows, d.hq, D)) != LOONG_OK) return st;
   BwdArgs a;
   a.batch = static_cast<int>(d.batch);
   a.S = static_cast<int>(d.seqlen);
@@ -571,7 +600,7 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
     a.t_begin = t_first;
     a.t_end = t_last;
     record_start(stream);
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, a);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, mdq, a);
     record_stop(stream);
     return check_launch();
   }
@@ -579,7 +608,7 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   for (int t = t_first; t < t_last; ++t) {
     a.t_begin = t;
     a.t_end = t + 1;
-    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, a);
+    kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, mo, mdq, a);
     if ((st = check_launch()) != LOONG_OK) return st;
   }
   record_stop(stream);

@@ -34,6 +34,10 @@ EncodeTiledFn tensor_map_encoder();
 // box (64, 1, 128), 128-byte swizzle.  Returns LOONG_OK or an error status.
 int make_head_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d);
 
+// fp32 tensor [rows][heads][d] viewed as (d, heads, rows), box (32, 1, 128),
+// 128-byte swizzle (one box row is 128 bytes).
+int make_f32_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d);
+
 RingGeom ring_geom(const loong_attn_desc& d);
 
 // Kernel launchers (asynchronous on `stream`).
