@@ -19,10 +19,11 @@
 // as soon as S^T is ready, while dP^T is still on the tensor cores, and drain
 // dQ while dK is computed.
 //
-// Warp roles (320 threads): warps 0-3 and 4-7 form two groups that each cover
+// Warp roles (352 threads): warps 0-3 and 4-7 form two groups that each cover
 // all 128 TMEM lanes; group w handles query columns [64w, 64w+64) of S^T/dP^T
 // and head-dim columns [D/2*w, D/2*(w+1)) of dQ; warp 8 issues TMA loads,
-// warp 9 allocates TMEM and issues the MMAs.
+// warp 9 allocates TMEM and issues the MMAs, warp 10 issues the dQ bulk
+// reductions (so no compute warp waits on their completion).
 // Tensor memory (512 columns): R0 [0,128) S^T, then P^T as bf16 pairs, each
 // group packing its 64 queries into the first 32 columns of its own half (the
 // two groups share lanes, so neither may write where the other still reads);
@@ -50,7 +51,7 @@ struct BwdCfg {
   // Tiles first (1024-byte aligned, checked at run time), then the row
   // statistics stages, the barriers, the TMEM base address and the abort flag.
   static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 352;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t R0 = 0, R1 = 128, RV = 256, RK = 256 + D;
   // dQ leaves through TMA bulk reductions of 32-float x 128-row boxes; the
@@ -85,7 +86,7 @@ struct BwdArgs {
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, bool STEP>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     ring_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
@@ -112,8 +113,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* dq_full = ds_full + 1;      // dQ(i) in R1           (MMA -> warps)
   uint64_t* dq_empty = dq_full + 1;     // R1 drained            (warps -> MMA)
   uint64_t* dk_done = dq_empty + 1;     // dK(i) done: Q/dO stage free for staging
-  uint64_t* staged = dk_done + 1;       // [2] a group's dQ boxes are in smem (warps -> its issuer)
-  uint64_t* acc_full = staged + 2;      // dK/dV ready to flush  (MMA -> warps)
+  uint64_t* staged = dk_done + 1;       // dQ(i) staged in smem  (warps -> reducer)
+  uint64_t* acc_full = staged + 1;      // dK/dV ready to flush  (MMA -> warps)
   uint64_t* acc_empty = acc_full + 1;   // dK/dV flushed         (warps -> MMA)
   uint64_t* done_bar = acc_empty + 1;
   uint64_t* drain = done_bar + 1;
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 2);  // both compute groups, after their dQ boxes are read
+      mbar_init(&q_empty[s], 1);  // the reducer, once the stage's dQ boxes are read
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -156,8 +157,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
     mbar_init(dk_done, 1);
-    mbar_init(&staged[0], 4);
-    mbar_init(&staged[1], 4);
+    mbar_init(staged, 8);
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
     mbar_init(done_bar, 1);
@@ -295,6 +295,29 @@ __global__ void __launch_bounds__(320, 1)
       mma_commit(drain);
       mbar_drain(drain, 0, a.err);
     }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ dQ reducer
+    // Adds each staged dQ tile into the fp32 accumulator with TMA bulk tensor
+    // reductions and hands the stage back to the producer once it is read.
+    if (lane == 0) {
+      for (int i = 0; i < n; ++i, walk.advance()) {
+        if (!mbar_wait(staged, i & 1, abort_flag, a.err)) break;
+        const int s = i % C::NS;
+        const int head = kvh * a.G + walk.head;
+#pragma unroll
+        for (int box = 0; box < C::DQ_BOXES; ++box) {
+          const uint8_t* base = box < C::BOXES_PER_STAGE
+                                    ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
+                                    : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
+          tma_reduce_add_3d(&tmDQ, base, box * 32, head, static_cast<int>(row_base + walk.q0()));
+        }
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(&q_empty[s]);
+      }
+      // the reductions must land before the kernel ends
+      bulk_wait_all();
+    }
   } else {
     // ------------------------------------------------------------ compute warps
     const int grp = warp >> 2;  // query columns [64 grp, 64 grp + 64)
@@ -326,12 +349,20 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_after();
       float pv[2][32];
+      {
+        uint32_t sv0[32], sv1[32];
+        tmem_ld32(tbase + t_lane + C::R0 + grp * 64, sv0);
+        tmem_ld32(tbase + t_lane + C::R0 + grp * 64 + 32, sv1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          pv[0][e] = __uint_as_float(sv0[e]);
+          pv[1][e] = __uint_as_float(sv1[e]);
+        }
+      }
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int cbase = grp * 64 + ch * 32;  // first query column of the chunk
-        uint32_t sv[32];
-        tmem_ld32(tbase + t_lane + C::R0 + cbase, sv);
-        tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -343,7 +374,7 @@ __global__ void __launch_bounds__(320, 1)
             const int c = cbase + e + u;
             const bool live = key_ok && c < qlen && (!dg || row <= c);
             // masked columns may hold statistics of other rows or padding: select
-            const float x = fast_exp2(fmaf(__uint_as_float(sv[e + u]), a.scale_log2, -lv[u]));
+            const float x = fast_exp2(fmaf(pv[ch][e + u], a.scale_log2, -lv[u]));
             pv[ch][e + u] = live ? x : 0.f;
           }
           pk[e / 2] = pack_bf16(pv[ch][e], pv[ch][e + 1]);
@@ -369,12 +400,14 @@ __global__ void __launch_bounds__(320, 1)
         break;
       }
       tc_fence_after();
+      uint32_t dpv2[2][32];
+      tmem_ld32(tbase + t_lane + C::R1 + grp * 64, dpv2[0]);
+      tmem_ld32(tbase + t_lane + C::R1 + grp * 64 + 32, dpv2[1]);
+      tmem_wait_ld();
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int cbase = grp * 64 + ch * 32;
-        uint32_t dpv[32];
-        tmem_ld32(tbase + t_lane + C::R1 + cbase, dpv);
-        tmem_wait_ld();
+        const uint32_t(&dpv)[32] = dpv2[ch];
         uint32_t dsk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -450,22 +483,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&staged[grp]);
-        // one thread per group issues the group's reductions once its four
-        // warps have staged (a bounded wait: never a plain barrier here)
-        if (quarter == 0 && lane == 0 && mbar_wait(&staged[grp], i & 1, abort_flag, a.err)) {
-#pragma unroll
-          for (int cb = 0; cb < D / 64; ++cb) {
-            const int box = grp * (D / 64) + cb;
-            const uint8_t* base = box < C::BOXES_PER_STAGE
-                                      ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
-                                      : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
-            tma_reduce_add_3d(&tmDQ, base, box * 32, head, static_cast<int>(row_base + q0));
-          }
-          bulk_commit_group();
-          bulk_wait_read_all();
-          mbar_arrive(&q_empty[s]);
-        }
+        if (lane == 0) mbar_arrive(staged);
       }
 
       // ---- every kFlush iterations: fold dV / dK into the fp32 accumulators
@@ -498,8 +516,6 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0) mbar_arrive(acc_empty);
       }
     }
-    // the dQ reductions this thread issued must land before the kernel ends
-    if (quarter == 0 && lane == 0) bulk_wait_all();
     // ---------------------------------------------------------- epilogue
     if (ok) ok = warp_wait(done_bar, 0);
     if (ok) {
