@@ -360,26 +360,42 @@ __global__ void __launch_bounds__(352, 1)
           pv[1][e] = __uint_as_float(sv1[e]);
         }
       }
+      // Query columns c with lo <= c < hi are live for this key row (causal
+      // diagonal, ragged query tile, key row past the block).  Interior tiles
+      // have every column live and skip the per-element mask.
+      const int lo = dg ? row : 0;
+      const int hi = key_ok ? qlen : 0;
+      const bool unmasked = __all_sync(0xffffffffu, lo == 0 && hi == kTile);
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         const int cbase = grp * 64 + ch * 32;  // first query column of the chunk
         uint32_t pk[16];
+        if (unmasked) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          // the same query indices in every lane: broadcast shared-memory reads
-          const float4 l4 = *reinterpret_cast<const float4*>(lse_row + cbase + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = cbase + e + u;
-            const bool live = key_ok && c < qlen && (!dg || row <= c);
-            // masked columns may hold statistics of other rows or padding: select
-            const float x = fast_exp2(fmaf(pv[ch][e + u], a.scale_log2, -lv[u]));
-            pv[ch][e + u] = live ? x : 0.f;
+          for (int e = 0; e < 32; e += 4) {
+            // the same query indices in every lane: broadcast shared-memory reads
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_row + cbase + e);
+            pv[ch][e] = fast_exp2(fmaf(pv[ch][e], a.scale_log2, -l4.x));
+            pv[ch][e + 1] = fast_exp2(fmaf(pv[ch][e + 1], a.scale_log2, -l4.y));
+            pv[ch][e + 2] = fast_exp2(fmaf(pv[ch][e + 2], a.scale_log2, -l4.z));
+            pv[ch][e + 3] = fast_exp2(fmaf(pv[ch][e + 3], a.scale_log2, -l4.w));
           }
-          pk[e / 2] = pack_bf16(pv[ch][e], pv[ch][e + 1]);
-          pk[e / 2 + 1] = pack_bf16(pv[ch][e + 2], pv[ch][e + 3]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_row + cbase + e);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int c = cbase + e + u;
+              // masked columns may hold statistics of other rows or padding: select
+              const float x = fast_exp2(fmaf(pv[ch][e + u], a.scale_log2, -lv[u]));
+              pv[ch][e + u] = (c >= lo && c < hi) ? x : 0.f;
+            }
+          }
         }
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16(pv[ch][e], pv[ch][e + 1]);
         // P^T (bf16 pairs) into this group's own half of R0, columns
         // [64 grp + 16 ch, +16): already read by this group, never read by the other.
         asm volatile(
@@ -416,9 +432,10 @@ __global__ void __launch_bounds__(352, 1)
           float ds[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            // pv is 0 on masked columns; D may be another row's or padding there
             const float p = pv[ch][e + u];
-            ds[u] = p != 0.f ? p * (__uint_as_float(dpv[e + u]) - dv4[u]) : 0.f;
+            const float x = p * (__uint_as_float(dpv[e + u]) - dv4[u]);
+            // masked columns: p is 0 and D may be another row's or padding
+            ds[u] = unmasked ? x : (p != 0.f ? x : 0.f);
           }
           dsk[e / 2] = pack_bf16(ds[0], ds[1]);
           dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
