@@ -61,6 +61,34 @@ def measured_peaks():
                 "source": "fallback"}
 
 
+# ------------------------------------------------------------------ ncu traffic
+KERNEL_SOURCES = ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "ring.cuh")
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "head_context_attention_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    record, or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256") != kernel_source_hash():
+        return None
+    ent = rec.get("kernels", {}).get(kernel, {}).get(workload)
+    return None if ent is None else int(ent["dram_bytes_per_launch"])
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
@@ -316,7 +344,9 @@ def run_gpu(args, w, rank, local, world, pg):
         "pct_of_peak": round(100.0 * tflops / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": f"ring_{dominant}_kernel", "achieved": round(dom_tf, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(dom_tf / peak, 4),
-                     "peak_kind": f"bf16 sustained, of {peaks['source']}", "traffic": None},
+                     "peak_kind": f"bf16 sustained, of {peaks['source']}",
+                     "traffic": recorded_traffic(f"ring_{dominant}_kernel", w.name),
+                     "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
         "kernels": {
             "ring_fwd_kernel": {"ms": round(f_ms, 3), "tflops": round(fwd_tf, 2),
                                 "frac_of_peak": round(fwd_tf / peak, 4)},

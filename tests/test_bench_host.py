@@ -73,3 +73,16 @@ def test_reference_arm_nonzero_rank_exits_quietly():
                         "--steps", "1", "--warmup", "0"], capture_output=True, text=True, env=env,
                        timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_recorded_traffic_follows_kernel_sources(monkeypatch):
+    """The committed ncu DRAM record is reported only for the kernel sources it
+    was taken on; any other source hash gives null traffic."""
+    rec = json.load(open(os.path.join(ROOT, "profiles", "roofline_traffic.json")))
+    ent = rec["kernels"]["ring_bwd_kernel"]["llama3-8b-s128k"]
+    assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha256"])
+    assert bench.recorded_traffic("ring_bwd_kernel", "llama3-8b-s128k") == ent["dram_bytes_per_launch"]
+    assert bench.recorded_traffic("ring_bwd_kernel", "no-such-workload") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 64)
+    assert bench.recorded_traffic("ring_bwd_kernel", "llama3-8b-s128k") is None
