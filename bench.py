@@ -89,6 +89,36 @@ def recorded_traffic(kernel, workload):
     return None if ent is None else int(ent["dram_bytes_per_launch"])
 
 
+# ------------------------------------------------------------------ merge
+def time_lse_merge(w, o, lse, stream, dev, reps=5):
+    """The n-way log-sum-exp merge on its own (outside the timed step, which
+    merges inside the attention kernels): n = 2 fp32 partials of every
+    (token, q-head) row of the workload, fp32 output; inputs exceed L2."""
+    import torch
+
+    from head_context_attention_gb300 import ops
+    rows = w.batch * w.seqlen * w.hq
+    o_parts = torch.empty((2, rows, w.head_dim), dtype=torch.float32, device=dev)
+    o_parts[0].copy_(o.reshape(rows, w.head_dim))
+    o_parts[1].copy_(o.reshape(rows, w.head_dim).flip(0))
+    lse_parts = torch.stack([lse.reshape(rows), lse.reshape(rows).flip(0) - 1.0])
+    o_out = torch.empty((rows, w.head_dim), dtype=torch.float32, device=dev)
+    lse_out = torch.empty(rows, dtype=torch.float32, device=dev)
+    for _ in range(2):
+        ops.loong_lse_merge(o_parts, lse_parts, o_out, lse_out, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        ops.loong_lse_merge(o_parts, lse_parts, o_out, lse_out, stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    nbytes = rows * (2 * (4 * w.head_dim + 4) + 4 * w.head_dim + 4)
+    del o_parts, lse_parts, o_out, lse_out
+    return {"ms": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes, "parts": 2,
+            "rows": rows}
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
@@ -312,6 +342,7 @@ def run_gpu(args, w, rank, local, world, pg):
         raise SystemExit(f"device status {st} in the timed region")
     ms_total = t_start.elapsed_time(t_stop)
     ms_total = max_over_ranks(pg, ms_total, dev)
+    merge_rec = time_lse_merge(w, o, lse, stream, dev)
     ms_step = ms_total / args.steps
     f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
     b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b) if do_bwd else 0.0
@@ -354,6 +385,7 @@ def run_gpu(args, w, rank, local, world, pg):
                                 "frac_of_peak": round(bwd_tf / peak, 4)},
             "headctx_pack_qkv": {"ms": round(p_ms, 3), "gbs": round(pack_gbs, 1),
                                  "frac_of_hbm": round(pack_gbs / peaks["hbm_gbs"], 4), "bytes": pack_bytes},
+            "lse_merge": dict(merge_rec, frac_of_hbm=round(merge_rec["gbs"] / peaks["hbm_gbs"], 4)),
         },
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,

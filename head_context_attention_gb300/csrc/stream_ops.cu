@@ -5,6 +5,7 @@
 // work.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "internal.h"
@@ -65,65 +66,167 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* 
     out[i] = __float2bfloat16_rn(in[i]);
 }
 
-// One thread per (row, 4-float vector).  Every thread of a row recomputes the
-// row's weights from the n LSE values (served from L1).
-template <bool OUT_BF16>
-__global__ void lse_merge_kernel(int64_t rows, int d, int n_parts, const float* __restrict__ o_parts,
+// Unsigned division by a divisor fixed for the launch, n < 2^31: the
+// multiply-and-shift method of Granlund and Montgomery ("Division by Invariant
+// Integers using Multiplication", 1994), with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, so that n / d = (umulhi(m, n) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.l = 0;
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - d)) / d + 1);
+  return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (__umulhi(f.m, n) + n) >> f.l;
+}
+
+// One lane segment per row: L = min(32, 2^ceil(log2 vpr)) lanes, 32 / L rows
+// per warp, each lane covering vectors lane, lane + L, ... of the row's
+// vpr = d / 4.  NP > 0 fixes the number of parts at compile time: the n LSE
+// values and the n 16-byte partial vectors are all loaded before any is used,
+// so a lane has 2n loads in flight.  NP = 0 is the general loop.  An empty
+// part (LSE = -inf) gets weight 0 and its partial is never combined.
+template <bool OUT_BF16, int NP>
+__global__ void lse_merge_kernel(int64_t rows, int d, int n_parts, int seg_log2, const float* __restrict__ o_parts,
                                  const float* __restrict__ lse_parts, void* __restrict__ o_out,
                                  float* __restrict__ lse_out) {
   const int vpr = d / 4;
-  const int64_t total = rows * vpr;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
-    const int64_t row = i / vpr;
-    const int vec = static_cast<int>(i - row * vpr);
-    float mx = -INFINITY;
-    for (int p = 0; p < n_parts; ++p) mx = fmaxf(mx, __ldg(lse_parts + p * rows + row));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
-    if (mx != -INFINITY) {
+  const int L = 1 << seg_log2;
+  const int sub = (threadIdx.x & 31) >> seg_log2;  // row within the warp
+  const int li = threadIdx.x & (L - 1);            // lane within the row
+  const int rows_per_warp = 32 >> seg_log2;
+  const int64_t warp_id = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int n = NP > 0 ? NP : n_parts;
+  for (int64_t row = warp_id * rows_per_warp + sub; row < rows; row += nwarps * rows_per_warp) {
+    float out_lse = -INFINITY;
+    if constexpr (NP > 0) {
+      // rows `row` and `row + step` together when a lane owns one vector per row
+      // and the parts are few (more loads in flight would cost occupancy)
+      const int64_t step = nwarps * rows_per_warp;
+      const bool pair = NP <= 2 && vpr <= L;
+      const int nr = pair && row + step < rows ? 2 : 1;
+      float l[2][NP];
+      float4 x[2][NP];
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        if (k < nr) {
+          const int64_t rk = row + k * step;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) l[k][p] = __ldg(lse_parts + p * rows + rk);
+        }
+      for (int v = li; v < vpr; v += L) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (k < nr) {
+            const int64_t rk = row + k * step;
+#pragma unroll
+            for (int p = 0; p < NP; ++p)
+              x[k][p] = __ldg(reinterpret_cast<const float4*>(o_parts + (p * rows + rk) * d) + v);
+          }
+        // weights formed after the loads are issued (lane 0 always has v = 0 and sets the LSE)
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          if (k < nr) {
+            const int64_t rk = row + k * step;
+            float mx = l[k][0];
+#pragma unroll
+            for (int p = 1; p < NP; ++p) mx = fmaxf(mx, l[k][p]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float lse_k = -INFINITY;
+            if (mx != -INFINITY) {
+              float w[NP], tot = 0.f;
+#pragma unroll
+              for (int p = 0; p < NP; ++p) {
+                w[p] = l[k][p] == -INFINITY ? 0.f : exp2f((l[k][p] - mx) * kLog2e);
+                tot += w[p];
+              }
+              const float inv = 1.f / tot;
+#pragma unroll
+              for (int p = 0; p < NP; ++p) {
+                if (w[p] != 0.f) {
+                  const float wp = w[p] * inv;
+                  acc.x = fmaf(wp, x[k][p].x, acc.x);
+                  acc.y = fmaf(wp, x[k][p].y, acc.y);
+                  acc.z = fmaf(wp, x[k][p].z, acc.z);
+                  acc.w = fmaf(wp, x[k][p].w, acc.w);
+                }
+              }
+              lse_k = mx + log2f(tot) * kLn2;
+            }
+            if (OUT_BF16) {
+              uint2 o2;
+              o2.x = pack_bf16(acc.x, acc.y);
+              o2.y = pack_bf16(acc.z, acc.w);
+              reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + rk * d)[v] = o2;
+            } else {
+              reinterpret_cast<float4*>(static_cast<float*>(o_out) + rk * d)[v] = acc;
+            }
+            if (v == 0) lse_out[rk] = lse_k;
+          }
+      }
+      if (nr == 2) row += step;  // the loop's own increment moves past the second row
+      continue;
+    } else {
+      float mx = -INFINITY;
+      for (int p = 0; p < n; ++p) mx = fmaxf(mx, __ldg(lse_parts + p * rows + row));
       float tot = 0.f;
-      for (int p = 0; p < n_parts; ++p) {
-        const float l = __ldg(lse_parts + p * rows + row);
-        const float w = l == -INFINITY ? 0.f : exp2f((l - mx) * kLog2e);
-        tot += w;
-        if (w != 0.f) {
-          const float4 x = __ldg(reinterpret_cast<const float4*>(o_parts + (p * rows + row) * d) + vec);
-          acc.x = fmaf(w, x.x, acc.x);
-          acc.y = fmaf(w, x.y, acc.y);
-          acc.z = fmaf(w, x.z, acc.z);
-          acc.w = fmaf(w, x.w, acc.w);
+      if (mx != -INFINITY)
+        for (int p = 0; p < n; ++p) {
+          const float l = __ldg(lse_parts + p * rows + row);
+          tot += l == -INFINITY ? 0.f : exp2f((l - mx) * kLog2e);
+        }
+      const float inv = mx != -INFINITY ? 1.f / tot : 0.f;
+      for (int v = li; v < vpr; v += L) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (mx != -INFINITY) {
+          for (int p = 0; p < n; ++p) {
+            const float l = __ldg(lse_parts + p * rows + row);
+            const float w = l == -INFINITY ? 0.f : exp2f((l - mx) * kLog2e) * inv;
+            if (w != 0.f) {
+              const float4 x = __ldg(reinterpret_cast<const float4*>(o_parts + (p * rows + row) * d) + v);
+              acc.x = fmaf(w, x.x, acc.x);
+              acc.y = fmaf(w, x.y, acc.y);
+              acc.z = fmaf(w, x.z, acc.z);
+              acc.w = fmaf(w, x.w, acc.w);
+            }
+          }
+        }
+        if (OUT_BF16) {
+          uint2 o2;
+          o2.x = pack_bf16(acc.x, acc.y);
+          o2.y = pack_bf16(acc.z, acc.w);
+          reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + row * d)[v] = o2;
+        } else {
+          reinterpret_cast<float4*>(static_cast<float*>(o_out) + row * d)[v] = acc;
         }
       }
-      const float inv = 1.f / tot;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-      lse = mx + log2f(tot) * kLn2;
+      if (mx != -INFINITY) out_lse = mx + log2f(tot) * kLn2;
     }
-    if (OUT_BF16) {
-      uint2 w;
-      w.x = pack_bf16(acc.x, acc.y);
-      w.y = pack_bf16(acc.z, acc.w);
-      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + row * d)[vec] = w;
-    } else {
-      reinterpret_cast<float4*>(static_cast<float*>(o_out) + row * d)[vec] = acc;
-    }
-    if (vec == 0) lse_out[row] = lse;
+    if (li == 0) lse_out[row] = out_lse;
   }
 }
 
 struct PackGeom {
-  int64_t batch, s_local, seqlen, blk;
+  int64_t batch, s_local, seqlen, blk, s_grp;  // s_grp = P * s_local, tokens per ring rank
   int cp, P, H, Hp, vpr;  // vpr: 16-byte vectors per (token, head) row
   int gather;             // 0 rank-major, 1 paired blocks, 2 contiguous blocks
+  int W;                  // 16-byte vectors per output row
+  int tile_rows;          // output rows per tile
+  FastDiv fW, fRv;        // division by W and by Hp * vpr
 };
 
 // Natural token of rank-local position u of ring rank c.
 __device__ __forceinline__ int64_t natural_token(const PackGeom& g, int c, int64_t u) {
   if (g.gather == 1) return u < g.blk ? c * g.blk + u : (2 * g.cp - 1 - c) * g.blk + (u - g.blk);
-  return c * (g.P * g.s_local) + u;
+  return c * g.s_grp + u;
 }
 
 // Rank-local (c, u) of natural token `tok`.
@@ -139,72 +242,87 @@ __device__ __forceinline__ void rank_local(const PackGeom& g, int64_t tok, int& 
       u = g.blk + off;
     }
   } else {
-    const int64_t sl = g.P * g.s_local;
-    c = static_cast<int>(tok / sl);
-    u = tok - c * sl;
+    c = static_cast<int>(tok / g.s_grp);
+    u = tok - c * g.s_grp;
   }
 }
 
-// Direction 0, enumerated over output vectors (coalesced writes).
-__global__ void pack_fwd_kernel(PackGeom g, const uint4* __restrict__ in, uint4* __restrict__ out) {
-  const int64_t S_grp = static_cast<int64_t>(g.P) * g.s_local;  // tokens per ring rank
-  const int64_t total = g.batch * g.cp * g.P * S_grp * g.Hp * g.vpr;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
-    int64_t x = i;
-    const int v = static_cast<int>(x % g.vpr);
-    x /= g.vpr;
-    const int hh = static_cast<int>(x % g.Hp);
-    x /= g.Hp;
-    const int64_t u = x % S_grp;
-    x /= S_grp;
-    const int p = static_cast<int>(x % g.P);
-    const int64_t n = x / g.P;
-    const int q = static_cast<int>(u / g.s_local);
-    const int64_t t = u - q * g.s_local;
-    const int head = p * g.Hp + hh;
-    int64_t src;
+// Both directions copy whole output rows, tile_rows at a time.  Direction 0:
+// output row (n, p, u) of [N][P][S_grp][Hp] is the contiguous head range
+// [p Hp, (p+1) Hp) of one input token row.  Direction 1: output token row
+// (all H heads) gathers P contiguous Hp-head runs, one per head rank p.  Each
+// row's source offset is formed once per tile in shared memory; the copy is
+// then 16-byte vectors with U loads in flight per thread and coalesced stores
+// (output rows of a tile are contiguous).
+template <int DIR>
+__device__ __forceinline__ int64_t pack_row_source(const PackGeom& g, int64_t row) {
+  if (DIR == 0) {
+    const int64_t u = row % g.s_grp;
+    const int64_t np = row / g.s_grp;
+    const int p = static_cast<int>(np % g.P);
+    const int64_t n = np / g.P;
+    int64_t tok_row;
     if (g.gather == 0) {
-      src = ((n * g.P + q) * g.s_local + t) * g.H + head;
+      tok_row = n * g.s_grp + u;  // [n][q][t] with u = q s_local + t
     } else {
       const int64_t b = n / g.cp;
-      const int c = static_cast<int>(n - b * g.cp);
-      src = (b * g.seqlen + natural_token(g, c, u)) * g.H + head;
+      tok_row = b * g.seqlen + natural_token(g, static_cast<int>(n - b * g.cp), u);
     }
-    out[i] = __ldg(in + src * g.vpr + v);
+    return (tok_row * g.H + static_cast<int64_t>(p) * g.Hp) * g.vpr;
   }
+  int64_t n, u;
+  if (g.gather == 0) {
+    n = row / g.s_grp;
+    u = row - n * g.s_grp;
+  } else {
+    const int64_t b = row / g.seqlen;
+    int c;
+    rank_local(g, row - b * g.seqlen, c, u);
+    n = b * g.cp + c;
+  }
+  return (n * g.P * g.s_grp + u) * static_cast<int64_t>(g.Hp) * g.vpr;
 }
 
-// Direction 1, enumerated over output vectors.
-__global__ void pack_inv_kernel(PackGeom g, const uint4* __restrict__ in, uint4* __restrict__ out) {
-  const int64_t S_grp = static_cast<int64_t>(g.P) * g.s_local;
-  const int64_t total = g.batch * g.cp * S_grp * g.H * g.vpr;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
-    int64_t x = i;
-    const int v = static_cast<int>(x % g.vpr);
-    x /= g.vpr;
-    const int head = static_cast<int>(x % g.H);
-    x /= g.H;
-    int64_t n, u;
-    if (g.gather == 0) {
-      // out rank-major [n][q][t][H]: x = (n*P + q)*s_local + t
-      const int64_t t = x % g.s_local;
-      x /= g.s_local;
-      const int q = static_cast<int>(x % g.P);
-      n = x / g.P;
-      u = q * g.s_local + t;
-    } else {
-      const int64_t tok = x % g.seqlen;
-      const int64_t b = x / g.seqlen;
-      int c;
-      rank_local(g, tok, c, u);
-      n = b * g.cp + c;
+constexpr int kPackThreads = 256;
+constexpr int kPackMaxRows = 256;
+
+template <int DIR>
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(PackGeom g, int64_t total_rows, const uint4* __restrict__ in,
+                                                           uint4* __restrict__ out) {
+  __shared__ int64_t src_row[kPackMaxRows];
+  constexpr int U = 8;
+  const int64_t ntiles = (total_rows + g.tile_rows - 1) / g.tile_rows;
+  const int64_t plane = g.s_grp * g.Hp * g.vpr;  // vectors per (n, p) plane of the packed layout
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    const int64_t row0 = tile * g.tile_rows;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(g.tile_rows), total_rows - row0));
+    __syncthreads();  // the previous tile's offsets are no longer read
+    for (int r = threadIdx.x; r < rows; r += kPackThreads) src_row[r] = pack_row_source<DIR>(g, row0 + r);
+    __syncthreads();
+    const int nvec = rows * g.W;
+    uint4* dst = out + row0 * g.W;
+    for (int j0 = threadIdx.x; j0 < nvec; j0 += kPackThreads * U) {
+      uint4 v[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int j = j0 + k * kPackThreads;
+        if (j < nvec) {
+          const uint32_t r = fdiv(static_cast<uint32_t>(j), g.fW);
+          const uint32_t w = static_cast<uint32_t>(j) - r * g.W;
+          int64_t off = w;
+          if (DIR == 1) {
+            const uint32_t p = fdiv(w, g.fRv);
+            off = p * plane + (w - p * g.fRv.d);
+          }
+          v[k] = __ldg(in + src_row[r] + off);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int j = j0 + k * kPackThreads;
+        if (j < nvec) dst[j] = v[k];
+      }
     }
-    const int p = head / g.Hp;
-    const int hh = head - p * g.Hp;
-    const int64_t src = ((n * g.P + p) * S_grp + u) * g.Hp + hh;
-    out[i] = __ldg(in + src * g.vpr + v);
   }
 }
 
@@ -270,14 +388,40 @@ int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t strea
   return check_launch();
 }
 
+template <bool OUT_BF16>
+void merge_dispatch(unsigned grid, cudaStream_t stream, int64_t rows, int d, int n_parts, int seg_log2,
+                    const float* o_parts, const float* lse_parts, void* o_out, float* lse_out) {
+  switch (n_parts) {
+    case 1:
+      lse_merge_kernel<OUT_BF16, 1><<<grid, 256, 0, stream>>>(rows, d, 1, seg_log2, o_parts, lse_parts, o_out, lse_out);
+      break;
+    case 2:
+      lse_merge_kernel<OUT_BF16, 2><<<grid, 256, 0, stream>>>(rows, d, 2, seg_log2, o_parts, lse_parts, o_out, lse_out);
+      break;
+    case 3:
+      lse_merge_kernel<OUT_BF16, 3><<<grid, 256, 0, stream>>>(rows, d, 3, seg_log2, o_parts, lse_parts, o_out, lse_out);
+      break;
+    case 4:
+      lse_merge_kernel<OUT_BF16, 4><<<grid, 256, 0, stream>>>(rows, d, 4, seg_log2, o_parts, lse_parts, o_out, lse_out);
+      break;
+    default:
+      lse_merge_kernel<OUT_BF16, 0><<<grid, 256, 0, stream>>>(rows, d, n_parts, seg_log2, o_parts, lse_parts, o_out,
+                                                              lse_out);
+  }
+}
+
 int launch_lse_merge(int64_t rows, int d, int n_parts, const float* o_parts, const float* lse_parts,
                      void* o_out, float* lse_out, int out_bf16, cudaStream_t stream) {
   if (rows == 0) return LOONG_OK;
-  const unsigned grid = grid_for(rows * (d / 4), 256, 8);
+  const int vpr = d / 4;
+  int seg_log2 = 0;
+  while ((1 << seg_log2) < vpr && seg_log2 < 5) ++seg_log2;
+  const int64_t rows_per_warp = 32 >> seg_log2;
+  const unsigned grid = grid_for((rows + rows_per_warp - 1) / rows_per_warp * 32, 256, 8);
   if (out_bf16)
-    lse_merge_kernel<true><<<grid, 256, 0, stream>>>(rows, d, n_parts, o_parts, lse_parts, o_out, lse_out);
+    merge_dispatch<true>(grid, stream, rows, d, n_parts, seg_log2, o_parts, lse_parts, o_out, lse_out);
   else
-    lse_merge_kernel<false><<<grid, 256, 0, stream>>>(rows, d, n_parts, o_parts, lse_parts, o_out, lse_out);
+    merge_dispatch<false>(grid, stream, rows, d, n_parts, seg_log2, o_parts, lse_parts, o_out, lse_out);
   return check_launch();
 }
 
@@ -286,7 +430,8 @@ int launch_headctx_pack(int64_t batch, int cp, int P, int64_t s_local, int heads
   PackGeom g;
   g.batch = batch;
   g.s_local = s_local;
-  g.seqlen = static_cast<int64_t>(cp) * P * s_local;
+  g.s_grp = static_cast<int64_t>(P) * s_local;
+  g.seqlen = static_cast<int64_t>(cp) * g.s_grp;
   g.blk = gather == 1 ? g.seqlen / (2 * cp) : g.seqlen / cp;
   g.cp = cp;
   g.P = P;
@@ -294,13 +439,23 @@ int launch_headctx_pack(int64_t batch, int cp, int P, int64_t s_local, int heads
   g.Hp = heads / P;
   g.vpr = d * 2 / 16;
   g.gather = gather;
-  const int64_t total = batch * g.seqlen * heads * g.vpr;
-  if (total == 0) return LOONG_OK;
-  const unsigned grid = grid_for(total, 256, 8);
+  const int64_t total_rows = direction == 0 ? batch * cp * P * g.s_grp : batch * g.seqlen;
+  if (total_rows == 0) return LOONG_OK;
+  const int64_t w = direction == 0 ? static_cast<int64_t>(g.Hp) * g.vpr : static_cast<int64_t>(heads) * g.vpr;
+  // a tile of about 2048 vectors (32 KB); the in-tile vector index stays in 32 bits
+  if (w > (1 << 20)) return LOONG_ERR_UNSUPPORTED;
+  g.W = static_cast<int>(w);
+  g.tile_rows = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kPackMaxRows, 2048 / w)));
+  g.fW = make_fastdiv(static_cast<uint32_t>(g.W));
+  g.fRv = make_fastdiv(static_cast<uint32_t>(g.Hp * g.vpr));
+  const int64_t ntiles = (total_rows + g.tile_rows - 1) / g.tile_rows;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(num_sms()) * 8));
   if (direction == 0)
-    pack_fwd_kernel<<<grid, 256, 0, stream>>>(g, static_cast<const uint4*>(in), static_cast<uint4*>(out));
+    pack_kernel<0><<<grid, kPackThreads, 0, stream>>>(g, total_rows, static_cast<const uint4*>(in),
+                                                      static_cast<uint4*>(out));
   else
-    pack_inv_kernel<<<grid, 256, 0, stream>>>(g, static_cast<const uint4*>(in), static_cast<uint4*>(out));
+    pack_kernel<1><<<grid, kPackThreads, 0, stream>>>(g, total_rows, static_cast<const uint4*>(in),
+                                                      static_cast<uint4*>(out));
   return check_launch();
 }
 

@@ -12,8 +12,14 @@ from tests.helpers import assert_close, to64
 pytestmark = pytest.mark.gpu
 
 
+# Rows beyond a few thousand reach the two-rows-per-lane path of n <= 2 (rows
+# past one grid stride); d = 256 gives lanes several vectors; n = 3, 4 are the
+# other fixed-count paths, n >= 5 the general loop.
 @pytest.mark.parametrize("rows,d,n,empty_frac", [(1, 4, 1, 0.0), (1000, 128, 2, 0.1),
-                                                 (777, 64, 5, 0.3), (4096, 128, 16, 0.05)])
+                                                 (777, 64, 5, 0.3), (4096, 128, 16, 0.05),
+                                                 (50001, 128, 2, 0.1), (40003, 64, 2, 0.5),
+                                                 (30000, 256, 3, 0.2), (20011, 32, 4, 0.0),
+                                                 (9001, 200, 1, 0.3)])
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_lse_merge_matches_oracle(cuda_device, rows, d, n, empty_frac, out_bf16):
     g = torch.Generator(device="cuda").manual_seed(rows + n)
@@ -22,10 +28,15 @@ def test_lse_merge_matches_oracle(cuda_device, rows, d, n, empty_frac, out_bf16)
     drop = torch.rand((n, rows), generator=g, device="cuda") < empty_frac
     lse_parts[drop] = -torch.inf
     lse_parts[:, :3] = -torch.inf if rows > 5 else lse_parts[:, :3]   # rows with every part empty
+    # an empty part is the merge's identity: whatever its O holds (NaN here)
+    # must never reach the result; the oracle is given zeros there
+    o_ref = to64(o_parts)
+    o_ref[to64(torch.isneginf(lse_parts)).astype(bool)] = 0.0
+    o_parts[torch.isneginf(lse_parts)] = float("nan")
     o_out = torch.empty((rows, d), dtype=torch.bfloat16 if out_bf16 else torch.float32, device="cuda")
     lse_out = torch.empty(rows, device="cuda")
     ops.loong_lse_merge(o_parts, lse_parts, o_out, lse_out)
-    want_o, want_l = merge.lse_merge(to64(o_parts), to64(lse_parts))
+    want_o, want_l = merge.lse_merge(o_ref, to64(lse_parts))
     tol = 1e-2 if out_bf16 else 1e-5
     assert_close("O", to64(o_out), want_o, tol, tol)
     gl, wl = to64(lse_out), want_l
@@ -36,7 +47,8 @@ def test_lse_merge_matches_oracle(cuda_device, rows, d, n, empty_frac, out_bf16)
 
 @pytest.mark.parametrize("B,S,H,d,cp,P,gather", [
     (1, 1024, 4, 128, 4, 2, 1), (1, 1024, 8, 64, 2, 4, 1), (2, 768, 6, 128, 3, 2, 1),
-    (1, 512, 8, 128, 4, 8, 2), (1, 256, 2, 8, 2, 2, 1), (1, 4096, 64, 128, 8, 8, 1)])
+    (1, 512, 8, 128, 4, 8, 2), (1, 256, 2, 8, 2, 2, 1), (1, 4096, 64, 128, 8, 8, 1),
+    (1, 512, 256, 128, 2, 4, 1), (3, 384, 12, 64, 2, 3, 2)])
 def test_headctx_pack_bit_exact(cuda_device, B, S, H, d, cp, P, gather):
     g = torch.Generator(device="cuda").manual_seed(S + H)
     x = torch.randn((B, S, H, d), generator=g, device="cuda").to(torch.bfloat16)
