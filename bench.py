@@ -1,13 +1,17 @@
 """Benchmark of the GB300 LoongTrain 2D-Attention ring step.
 
-One step = one pass of the hot path over one batch of synthetic input: the
-Ulysses head-context repack of Q, K and V ((S/P, H) -> (S, H/P) for every ring
-rank's head group), the fused ring-attention forward (online softmax merged
-over the double-ring schedule) and the backward (row statistics, dQ/dK/dV).
+One step = one pass of the 2D-attention hot path over one batch of synthetic
+input (default ``--layout rank-major``): the Ulysses head-context repack of Q,
+K, V and dO from the natural layout into every emulated rank's (S/cp, H/hp)
+layout, the fused ring-attention forward (online softmax merged over the
+double-ring schedule) and backward (row statistics, dQ/dK/dV) reading and
+writing that layout, and the repack of O, dQ, dK, dV back.  ``--layout
+natural`` runs the ring kernels on the natural layout with no repack.
 Metric: algorithmic causal TFLOP/s of forward + backward, 7 * B * S^2 * Hq * d
 per step (forward 2 GEMMs over the causal half, backward 2.5x the forward).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--layout rank-major|natural] [--mode fused|stepwise]
                     [--impl reference] [--no-e2e] [--no-cpu-baseline]
 
 Under torchrun each rank runs the whole workload on its own GPU as an
@@ -40,7 +44,11 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
+    p.add_argument("--layout", default="rank-major", choices=["rank-major", "natural"],
+                   help="rank-major: the step repacks in and out around the ring kernels (2D attention)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--per-rank", action=argparse.BooleanOptionalAction, default=True,
+                   help="after the timed steps, time each emulated ring rank's forward on its own")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
     p.add_argument("--seqlen", type=int, default=0,
@@ -74,9 +82,9 @@ def kernel_source_hash():
     return h.hexdigest()
 
 
-def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    record, or None when absent or taken on other kernel sources."""
+def recorded_traffic(kernel, workload, layout="rank-major"):
+    """DRAM bytes per launch of `kernel` on `workload` in `layout` from the
+    committed ncu record, or None when absent or taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
     try:
         with open(path) as f:
@@ -85,7 +93,7 @@ def recorded_traffic(kernel, workload):
         return None
     if rec.get("source_sha256") != kernel_source_hash():
         return None
-    ent = rec.get("kernels", {}).get(kernel, {}).get(workload)
+    ent = rec.get("kernels", {}).get(kernel, {}).get(workload, {}).get(layout)
     return None if ent is None else int(ent["dram_bytes_per_launch"])
 
 
@@ -117,6 +125,54 @@ def time_lse_merge(w, o, lse, stream, dev, reps=5):
     del o_parts, lse_parts, o_out, lse_out
     return {"ms": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes, "parts": 2,
             "rows": rows}
+
+
+# ------------------------------------------------------------------ per-rank work
+def rank_pairs(w, placement, c):
+    """Causal (query, key) pairs of ring rank c's query rows, per head: the
+    work the rank's share of the ring pass holds (query i sees keys 0..i)."""
+    nb = 2 * w.cp if placement == 1 else w.cp
+    L = w.seqlen // nb
+    blocks = (c, 2 * w.cp - 1 - c) if placement == 1 else (c,)
+    # rows of block j are j*L .. j*L + L - 1; row i sees i + 1 keys
+    return sum(L * (j * L) + L * (L + 1) // 2 for j in blocks)
+
+
+def time_per_rank(w, x, stream, dev, reps=3):
+    """Forward time of every emulated ring rank's query rows on its own
+    (loong_attn_fwd_ranks), FUSED, natural layout, for the paired-block and the
+    contiguous placement of the same workload, beside each rank's share of the
+    causal work."""
+    import torch
+
+    from head_context_attention_gb300 import ops
+
+    res = {}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=dev)
+    for name, pl in (("zigzag", ops.PLACEMENT_ZIGZAG), ("contiguous", ops.PLACEMENT_CONTIGUOUS)):
+        wp = w.with_(placement=pl)
+        desc = ops.make_desc(wp, ops.MODE_FUSED)
+        if ops.loong_attn_check(desc) != ops.LOONG_OK:
+            continue
+        ms = []
+        for c in range(w.cp):
+            ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, stream)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for a, b in ev:
+                a.record(stream)
+                ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, stream)
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(statistics.median(a.elapsed_time(b) for a, b in ev))
+        work = [rank_pairs(w, pl, c) for c in range(w.cp)]
+        tot_ms, tot_w = sum(ms), sum(work)
+        res[name] = {"ms": [round(m, 3) for m in ms],
+                     "time_share": [round(m / tot_ms, 4) for m in ms],
+                     "work_share": [round(u / tot_w, 4) for u in work],
+                     "max_over_mean_time": round(max(ms) * len(ms) / tot_ms, 3),
+                     "max_over_mean_work": round(max(work) * len(work) / tot_w, 3)}
+    return res
 
 
 # ------------------------------------------------------------------ clocks
@@ -263,6 +319,93 @@ def cpu_sample(w, seconds, arrays):
 
 
 # ------------------------------------------------------------------ GPU arm
+class TwoDPath:
+    """One fwd+bwd pass of 2D attention through the library's C entry points.
+
+    rank-major: Q, K, V, dO arrive in the natural [B, S, H, d] layout; the
+    Ulysses repack (loong_headctx_pack, paired- or contiguous-block gather)
+    moves them into the per-rank layout [B*cp, hp, S/cp, H/hp, d]; the ring
+    forward and backward read and write that layout (LAYOUT_RANK_MAJOR); O, dQ,
+    dK, dV are packed back to the natural layout.  natural: the ring kernels on
+    the natural layout directly, no repack."""
+
+    def __init__(self, w, mode, layout, dev, stream):
+        import torch
+
+        from head_context_attention_gb300 import ops
+
+        self.ops, self.w, self.stream = ops, w, stream
+        self.rank_major = layout == "rank-major"
+        self.desc = ops.make_desc(w, mode, layout=ops.LAYOUT_RANK_MAJOR if self.rank_major else ops.LAYOUT_NATURAL)
+        st = ops.loong_attn_check(self.desc)
+        if st != ops.LOONG_OK:
+            raise SystemExit(f"workload {w.name} rejected: {st}")
+        self.ws0, self.ws1 = ops.workspace(self.desc, 0, dev), ops.workspace(self.desc, 1, dev)
+        self.gather = 1 if w.placement == ops.PLACEMENT_ZIGZAG else 2
+        self.s_local = w.seqlen // (w.cp * w.hp)
+        B, S, d = w.batch, w.seqlen, w.head_dim
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        nat = {"q": w.hq, "o": w.hq, "do": w.hq, "dq": w.hq, "k": w.hkv, "v": w.hkv, "dk": w.hkv, "dv": w.hkv}
+        self.heads = nat
+        # natural-layout outputs, and the tensors the ring kernels use
+        self.out = {n: torch.empty((B, S, nat[n], d), **bf) for n in ("o", "dq", "dk", "dv")}
+        self.lse = torch.empty((B, w.hq, S), dtype=torch.float32, device=dev)
+        if self.rank_major:
+            self.kt = {n: torch.empty((B * w.cp, w.hp, S // w.cp, h // w.hp, d), **bf) for n, h in nat.items()}
+        self.do_bwd = w.backward
+
+    def launches(self):
+        ops, w = self.ops, self.w
+        fused = self.desc.mode == ops.MODE_FUSED
+        n = (1 if fused else w.cp + 2) + (((3 if fused else w.cp + 4)) if self.do_bwd else 0)
+        if self.rank_major:
+            n += (4 if self.do_bwd else 3) + (4 if self.do_bwd else 1)
+        return n
+
+    def pack_in(self, x):
+        if not self.rank_major:
+            return
+        names = ("q", "k", "v", "do") if self.do_bwd else ("q", "k", "v")
+        for n in names:
+            self._pack(x[n], self.kt[n], n, 0)
+
+    def _pack(self, src, dst, n, direction):
+        w = self.w
+        self.ops.loong_headctx_pack(src, dst, w.batch, w.cp, w.hp, self.s_local, self.heads[n], w.head_dim,
+                                    direction, self.gather, self.stream)
+
+    def fwd(self, x):
+        t = self.kt if self.rank_major else x
+        o = self.kt["o"] if self.rank_major else self.out["o"]
+        self.ops.loong_attn_fwd(self.desc, t["q"], t["k"], t["v"], o, self.lse, self.ws0, self.stream)
+
+    def bwd(self, x):
+        if not self.do_bwd:
+            return
+        t = self.kt if self.rank_major else x
+        g = self.kt if self.rank_major else self.out
+        o = self.kt["o"] if self.rank_major else self.out["o"]
+        self.ops.loong_attn_bwd(self.desc, t["q"], t["k"], t["v"], o, self.lse, t["do"], g["dq"], g["dk"],
+                                g["dv"], self.ws1, self.stream)
+
+    def unpack_out(self):
+        if not self.rank_major:
+            return
+        names = ("o", "dq", "dk", "dv") if self.do_bwd else ("o",)
+        for n in names:
+            self._pack(self.kt[n], self.out[n], n, 1)
+
+    def repack_bytes(self):
+        """Algorithmic bytes of the repacks of one step (read + write), in and out."""
+        w = self.w
+        if not self.rank_major:
+            return 0, 0
+        row = 2 * w.batch * w.seqlen * w.head_dim * 2
+        h_in = 2 * w.hq + 2 * w.hkv if self.do_bwd else w.hq + 2 * w.hkv
+        h_out = 2 * w.hq + 2 * w.hkv if self.do_bwd else w.hq
+        return row * h_in, row * h_out
+
+
 def run_gpu(args, w, rank, local, world, pg):
     import torch
 
@@ -271,37 +414,18 @@ def run_gpu(args, w, rank, local, world, pg):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     mode = ops.MODE_FUSED if args.mode == "fused" else ops.MODE_STEPWISE
-    desc = ops.make_desc(w, mode)
-    if ops.loong_attn_check(desc) != ops.LOONG_OK:
-        raise SystemExit(f"workload {w.name} rejected: {ops.loong_attn_check(desc)}")
-    x = inputs.make_inputs(w, device=dev, with_do=True)
-    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
-    o = torch.empty_like(q)
-    lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws0 = ops.workspace(desc, 0, dev)
-    ws1 = ops.workspace(desc, 1, dev)
-    P = w.hp
-    s_local = w.seqlen // (w.cp * P)
-    packed = {n: torch.empty((w.batch * w.cp, P, w.seqlen // w.cp, t.shape[2] // P, w.head_dim),
-                             dtype=torch.bfloat16, device=dev) for n, t in (("q", q), ("k", k), ("v", v))}
     stream = torch.cuda.current_stream(dev)
-
-    def repack():
-        for n, t in (("q", q), ("k", k), ("v", v)):
-            ops.loong_headctx_pack(t, packed[n], w.batch, w.cp, P, s_local, t.shape[2], w.head_dim, 0, 1,
-                                   stream)
-
+    path = TwoDPath(w, mode, args.layout, dev, stream)
+    x = inputs.make_inputs(w, device=dev, with_do=True)
     do_bwd = w.backward
+    # pinned host buffers of the end-to-end leg, taken before any timed work
+    e2e_bufs = None if args.no_e2e else pinned_buffers(w, path, x)
 
     def step():
-        repack()
-        ops.loong_attn_fwd(desc, q, k, v, o, lse, ws0, stream)
-        if do_bwd:
-            ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
-
-    launches_per_step = 3 + (1 if mode == ops.MODE_FUSED else w.cp + 2) + \
-        ((3 if mode == ops.MODE_FUSED else w.cp + 4) if do_bwd else 0)
+        path.pack_in(x)
+        path.fwd(x)
+        path.bwd(x)
+        path.unpack_out()
 
     for _ in range(args.warmup):
         step()
@@ -311,9 +435,9 @@ def run_gpu(args, w, rank, local, world, pg):
         raise SystemExit(f"device status {st} after warm-up")
 
     # Timed region: K steps; per-kernel events for the forward and backward kernels.
-    ev_f = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ev_b = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ev_p = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+    ev_f, ev_b, ev_p, ev_u = mk(), mk(), mk(), mk()
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # torch creates events lazily and tracks recording itself: record each once
     # here so the handle exists (the library re-records it around its kernels).
@@ -326,14 +450,17 @@ def run_gpu(args, w, rank, local, world, pg):
         t_start.record(stream)
         for i in range(args.steps):
             ev_p[i][0].record(stream)
-            repack()
+            path.pack_in(x)
             ev_p[i][1].record(stream)
             ops.loong_set_timing_events(*ev_f[i])
-            ops.loong_attn_fwd(desc, q, k, v, o, lse, ws0, stream)
+            path.fwd(x)
             if do_bwd:
                 ops.loong_set_timing_events(*ev_b[i])
-                ops.loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, ws1, stream)
+                path.bwd(x)
             ops.loong_set_timing_events(None, None)
+            ev_u[i][0].record(stream)
+            path.unpack_out()
+            ev_u[i][1].record(stream)
         t_stop.record(stream)
         torch.cuda.synchronize(dev)
     barrier(pg)
@@ -342,11 +469,13 @@ def run_gpu(args, w, rank, local, world, pg):
         raise SystemExit(f"device status {st} in the timed region")
     ms_total = t_start.elapsed_time(t_stop)
     ms_total = max_over_ranks(pg, ms_total, dev)
-    merge_rec = time_lse_merge(w, o, lse, stream, dev)
+    merge_rec = time_lse_merge(w, path.out["o"], path.lse, stream, dev)
+    per_rank = time_per_rank(w, x, stream, dev) if args.per_rank else None
     ms_step = ms_total / args.steps
     f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
     b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b) if do_bwd else 0.0
     p_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_p)
+    u_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_u)
     peaks = measured_peaks()
     flops_step = w.flops
     tflops = flops_step * world / (ms_step * 1e-3) / 1e12
@@ -354,13 +483,23 @@ def run_gpu(args, w, rank, local, world, pg):
     bwd_flops = w.fwd_flops * 2.5
     bwd_tf = bwd_flops / (b_ms * 1e-3) / 1e12 if do_bwd else 0.0
     fwd_tf = w.fwd_flops / (f_ms * 1e-3) / 1e12
-    pack_bytes = 2 * w.batch * w.seqlen * (w.hq + 2 * w.hkv) * w.head_dim * 2
-    pack_gbs = pack_bytes / (p_ms * 1e-3) / 1e9
+    in_bytes, out_bytes = path.repack_bytes()
     dominant = "bwd" if b_ms >= f_ms else "fwd"
     dom_tf = bwd_tf if dominant == "bwd" else fwd_tf
     peak = peaks["bf16_tflops_sustained"]
     clocks = clk.summary()
 
+    kernels = {
+        "ring_fwd_kernel": {"ms": round(f_ms, 3), "tflops": round(fwd_tf, 2), "frac_of_peak": round(fwd_tf / peak, 4)},
+        "ring_bwd_kernel": {"ms": round(b_ms, 3), "tflops": round(bwd_tf, 2), "frac_of_peak": round(bwd_tf / peak, 4)},
+    }
+    if path.rank_major:
+        for key, ms, nbytes, what in (("headctx_pack_in", p_ms, in_bytes, "Q, K, V, dO natural -> rank-major"),
+                                      ("headctx_pack_out", u_ms, out_bytes, "O, dQ, dK, dV rank-major -> natural")):
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            kernels[key] = {"ms": round(ms, 3), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                            "bytes": nbytes, "tensors": what}
+    kernels["lse_merge"] = dict(merge_rec, frac_of_hbm=round(merge_rec["gbs"] / peaks["hbm_gbs"], 4))
     result = {
         "metric": METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
@@ -369,27 +508,24 @@ def run_gpu(args, w, rank, local, world, pg):
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "hq": w.hq, "hkv": w.hkv,
                    "head_dim": w.head_dim, "hp": w.hp, "cp": w.cp, "ring_inner": w.ring_inner,
                    "ring_outer": w.ring_outer, "placement": "zigzag" if w.placement == 1 else "contiguous",
-                   "mode": args.mode, "parallelism": f"replicas x{world} (each rank: all hp x cp ranks emulated)",
+                   "mode": args.mode, "layout": args.layout,
+                   "step": ("repack Q,K,V,dO -> ring fwd + bwd on the rank-major layout -> repack O,dQ,dK,dV"
+                            if path.rank_major else "ring fwd + bwd on the natural layout"),
+                   "parallelism": f"replicas x{world} (each rank: all hp x cp ranks emulated)",
                    "l2": "inputs exceed L2 (Q and dO 1 GiB each at this size); no flush",
                    "flops_per_step": flops_step},
         "pct_of_peak": round(100.0 * tflops / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": f"ring_{dominant}_kernel", "achieved": round(dom_tf, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(dom_tf / peak, 4),
                      "peak_kind": f"bf16 sustained, of {peaks['source']}",
-                     "traffic": recorded_traffic(f"ring_{dominant}_kernel", w.name),
+                     "traffic": recorded_traffic(f"ring_{dominant}_kernel", w.name, args.layout),
                      "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
-        "kernels": {
-            "ring_fwd_kernel": {"ms": round(f_ms, 3), "tflops": round(fwd_tf, 2),
-                                "frac_of_peak": round(fwd_tf / peak, 4)},
-            "ring_bwd_kernel": {"ms": round(b_ms, 3), "tflops": round(bwd_tf, 2),
-                                "frac_of_peak": round(bwd_tf / peak, 4)},
-            "headctx_pack_qkv": {"ms": round(p_ms, 3), "gbs": round(pack_gbs, 1),
-                                 "frac_of_hbm": round(pack_gbs / peaks["hbm_gbs"], 4), "bytes": pack_bytes},
-            "lse_merge": dict(merge_rec, frac_of_hbm=round(merge_rec["gbs"] / peaks["hbm_gbs"], 4)),
-        },
+        "kernels": kernels,
         "clocks": clocks,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": path.launches() * args.steps,
     }
+    if per_rank is not None:
+        result["per_rank_fwd"] = per_rank
     rejected = [r for r in clocks.get("reasons", []) if r in SLOWDOWN_REASONS]
     if rejected:
         result["clocks"]["rejected"] = rejected
@@ -398,52 +534,71 @@ def run_gpu(args, w, rank, local, world, pg):
         del result["kernels"]["ring_bwd_kernel"]
         result["config"]["pass"] = "forward only"
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, w, desc, dev, stream, world, pg, x)
+        result["e2e"] = run_e2e(args, w, path, dev, stream, world, pg, x, e2e_bufs)
     return result, x
 
 
-def run_e2e(args, w, desc, dev, stream, world, pg, x):
-    """Same metric through the public API with host buffers: every step copies
-    Q, K, V, dO from pinned host memory and O, LSE, dQ, dK, dV back."""
+def pinned_buffers(w, path, x):
+    """Pinned host copies of the inputs and pinned host buffers for the outputs."""
     import torch
 
-    from head_context_attention_gb300 import ops
+    host_in = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in x.items()}
+    for n, t in x.items():
+        host_in[n].copy_(t)
+    outs = dict(path.out, lse=path.lse)
+    if not w.backward:
+        outs = {"o": path.out["o"], "lse": path.lse}
+    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+    return host_in, host_out, outs
 
-    host_in = {n: t.cpu().pin_memory() for n, t in x.items()}
+
+def run_e2e(args, w, path, dev, stream, world, pg, x, bufs):
+    """Same metric through the public API with host buffers: every step copies
+    Q, K, V, dO (natural layout) from pinned host memory and O, LSE, dQ, dK, dV
+    (natural layout) back, around the same pass as the timed step."""
+    import torch
+
+    host_in, host_out, outs = bufs
     dev_in = {n: torch.empty_like(t) for n, t in x.items()}
-    o = torch.empty_like(dev_in["q"])
-    lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(o), torch.empty_like(dev_in["k"]), torch.empty_like(dev_in["v"])
-    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-    ws0, ws1 = ops.workspace(desc, 0, dev), ops.workspace(desc, 1, dev)
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
-    def step():
+    phases = ("h2d", "repack_in", "fwd", "bwd", "repack_out", "d2h")
+
+    def step(ev=None):
+        mark = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        mark(0)
         for n in dev_in:
             dev_in[n].copy_(host_in[n], non_blocking=True)
-        ops.loong_attn_fwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, ws0, stream)
-        if w.backward:
-            ops.loong_attn_bwd(desc, dev_in["q"], dev_in["k"], dev_in["v"], o, lse, dev_in["do"], dq, dk, dv,
-                               ws1, stream)
+        mark(1)
+        path.pack_in(dev_in)
+        mark(2)
+        path.fwd(dev_in)
+        mark(3)
+        path.bwd(dev_in)
+        mark(4)
+        path.unpack_out()
+        mark(5)
         for n in host_out:
             host_out[n].copy_(outs[n], non_blocking=True)
+        mark(6)
 
     for _ in range(max(1, args.warmup)):
         step()
     torch.cuda.synchronize(dev)
     barrier(pg)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        step(evs[i])
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(pg, a.elapsed_time(b), dev) / args.steps
+    phase_ms = {p: round(statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs), 3) for j, p in enumerate(phases)}
     return {"value": round(w.flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "phase_ms": phase_ms}
 
 
 def main(argv=None):

@@ -160,13 +160,26 @@ RingGeom ring_geom(const loong_attn_desc& d) {
   return g;
 }
 
+Layout layout_of(const loong_attn_desc& d) {
+  const RingGeom g = ring_geom(d);
+  Layout l;
+  l.rank_major = d.layout == LOONG_LAYOUT_RANK_MAJOR;
+  l.P = d.hp;
+  l.cp = d.cp;
+  l.zigzag = g.zigzag;
+  l.blk = g.blk;
+  l.S = d.seqlen;
+  l.s_rank = d.seqlen / d.cp;
+  return l;
+}
+
 }  // namespace loong
 
 using namespace loong;
 
 extern "C" {
 
-int loong_version(void) { return (0 << 16) | 1; }
+int loong_version(void) { return (0 << 16) | 2; }
 
 const char* loong_status_string(int status) {
   switch (status) {
@@ -192,10 +205,13 @@ int loong_attn_check(const loong_attn_desc* d) {
   if (d->placement != LOONG_PLACEMENT_ZIGZAG && d->placement != LOONG_PLACEMENT_CONTIGUOUS)
     return LOONG_ERR_INVALID_ARG;
   if (d->mode != LOONG_MODE_FUSED && d->mode != LOONG_MODE_STEPWISE) return LOONG_ERR_INVALID_ARG;
+  if (d->layout != LOONG_LAYOUT_NATURAL && d->layout != LOONG_LAYOUT_RANK_MAJOR) return LOONG_ERR_INVALID_ARG;
   const int64_t nblocks = d->placement == LOONG_PLACEMENT_ZIGZAG ? 2 * static_cast<int64_t>(d->cp) : d->cp;
   if (d->seqlen % nblocks) return LOONG_ERR_INVALID_ARG;
   if ((d->seqlen / nblocks) % d->hp) return LOONG_ERR_INVALID_ARG;
-  if (d->batch * d->seqlen > 0x7fffffffLL) return LOONG_ERR_UNSUPPORTED;  // TMA row coordinate is int32
+  // TMA row coordinates are int32: rows of the [rows, heads, d] view
+  const int64_t view_rows = d->batch * d->seqlen * (d->layout == LOONG_LAYOUT_RANK_MAJOR ? d->hp : 1);
+  if (d->batch * d->seqlen > 0x7fffffffLL || view_rows > 0x7fffffffLL) return LOONG_ERR_UNSUPPORTED;
   if (!std::isfinite(d->softmax_scale)) return LOONG_ERR_INVALID_ARG;
   if (!is_pow2_ok_hd(d->head_dim)) return LOONG_ERR_UNSUPPORTED;
   if (d->causal != 1) return LOONG_ERR_UNSUPPORTED;
@@ -242,6 +258,19 @@ int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const
   if ((st = launch_fill_f32(lse, d->batch * d->hq * d->seqlen, -INFINITY, stream)) != LOONG_OK) return st;
   if ((st = launch_fwd(*d, q, k, v, o, lse, o_acc, stream)) != LOONG_OK) return st;
   return launch_f32_to_bf16(o_acc, o, q_elems, stream);
+}
+
+int loong_attn_fwd_ranks(const loong_attn_desc* d, int32_t rank_begin, int32_t rank_end, const void* q,
+                         const void* k, const void* v, void* o, float* lse, loong_stream_t stream_) {
+  int st = loong_attn_check(d);
+  if (st != LOONG_OK) return st;
+  if (d->mode != LOONG_MODE_FUSED) return LOONG_ERR_UNSUPPORTED;
+  if (rank_begin < 0 || rank_end <= rank_begin || rank_end > d->cp) return LOONG_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return LOONG_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return LOONG_ERR_INVALID_ARG;
+  if ((st = device_ready()) != LOONG_OK) return st;
+  return launch_fwd(*d, q, k, v, o, lse, nullptr, reinterpret_cast<cudaStream_t>(stream_), rank_begin, rank_end);
 }
 
 int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, const void* o,

@@ -69,16 +69,17 @@ constexpr int kFlush = 512;
 struct BwdArgs {
   int batch, S, hq, hkv, G;
   RingGeom ring;
+  Layout lay;  // where Q, K, V, dO, dQ (and its accumulator), dK, dV keep (token, head)
   int t_begin, t_end;
   float scale, scale_log2;
   // Row statistics, [B*Hq][stat_len] each, block b's rows at b*blk_pad:
   const float* lse2;   // LSE * log2(e)
   const float* dstat;  // D = rowsum(dO * O)
   int blk_pad, stat_len;
-  float* dq_acc;      // [B, S, Hq, D] fp32
+  float* dq_acc;      // fp32, the layout of Q
   __nv_bfloat16* dk;  // FUSED outputs
   __nv_bfloat16* dv;
-  float* dk_acc;      // fp32 accumulators [B, S, Hkv, D] (zeroed by the launcher)
+  float* dk_acc;      // fp32 accumulators, the layout of K (zeroed by the launcher)
   float* dv_acc;
   unsigned* err;
 };
@@ -180,27 +181,30 @@ __global__ void __launch_bounds__(352, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_sh;
-  const int64_t row_base = static_cast<int64_t>(b) * a.S;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(kv_full, 2 * C::TILE_BYTES);
+      int kvc;
+      const int kr = static_cast<int>(a.lay.view_row(b, k0, kvh, a.hkv, kvc));
       for (int at = 0; at < C::ATOMS; ++at) {
-        tma_load_3d(sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvh, static_cast<int>(row_base + k0));
-        tma_load_3d(sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvh, static_cast<int>(row_base + k0));
+        tma_load_3d(sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvc, kr);
+        tma_load_3d(sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvc, kr);
       }
       int issued = 0;
       for (int i = 0; i < n; ++i, walk.advance()) {
         const int s = i % C::NS;
         const int u = i / C::NS;
-        if (i >= C::NS && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
+        // coordinates first, off the wait's critical path
         const int head = kvh * a.G + walk.head;
-        const int qrow = static_cast<int>(row_base + walk.q0());
+        int hc;
+        const int qrow = static_cast<int>(a.lay.view_row(b, walk.q0(), head, a.hq, hc));
+        if (i >= C::NS && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         mbar_expect_tx(&q_full[s], 2 * C::TILE_BYTES + C::STAT_BYTES);
         for (int at = 0; at < C::ATOMS; ++at) {
-          tma_load_3d(sQ + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, &q_full[s], at * 64, head, qrow);
-          tma_load_3d(sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, head, qrow);
+          tma_load_3d(sQ + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, &q_full[s], at * 64, hc, qrow);
+          tma_load_3d(sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, hc, qrow);
         }
         // this tile's row statistics: 16-byte aligned and in bounds by construction
         const int64_t srow = (static_cast<int64_t>(b) * a.hq + head) * a.stat_len + walk.bq * a.blk_pad +
@@ -301,15 +305,17 @@ __global__ void __launch_bounds__(352, 1)
     // reductions and hands the stage back to the producer once it is read.
     if (lane == 0) {
       for (int i = 0; i < n; ++i, walk.advance()) {
-        if (!mbar_wait(staged, i & 1, abort_flag, a.err)) break;
         const int s = i % C::NS;
         const int head = kvh * a.G + walk.head;
+        int hc;
+        const int qrow = static_cast<int>(a.lay.view_row(b, walk.q0(), head, a.hq, hc));
+        if (!mbar_wait(staged, i & 1, abort_flag, a.err)) break;
 #pragma unroll
         for (int box = 0; box < C::DQ_BOXES; ++box) {
           const uint8_t* base = box < C::BOXES_PER_STAGE
                                     ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
                                     : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
-          tma_reduce_add_3d(&tmDQ, base, box * 32, head, static_cast<int>(row_base + walk.q0()));
+          tma_reduce_add_3d(&tmDQ, base, box * 32, hc, qrow);
         }
         bulk_commit_group();
         bulk_wait_read_all();
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(352, 1)
     const int row = quarter * 32 + lane;  // key row in the pass, query row in the dQ drain
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const bool key_ok = row < klen;
-    const int64_t krow = (row_base + k0 + row) * a.hkv + kvh;
+    const int64_t krow = a.lay.vec(b, k0 + row, kvh, a.hkv);  // this key row's d-vector in K / dK / dV
     // group 0 owns dV, group 1 owns dK (keys on lanes)
     const uint32_t acc_col = grp == 0 ? C::RV : C::RK;
     float* acc_glob = (grp == 0 ? a.dv_acc : a.dk_acc) + krow * D;
@@ -594,16 +600,19 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
                  const float* stats, float* dq_acc, void* dk, void* dv, float* dk_acc,
                  float* dv_acc, cudaStream_t stream) {
   using C = BwdCfg<D>;
-  const int64_t rows = d.batch * d.seqlen;
+  const Layout lay = layout_of(d);
+  const int64_t rows = lay.view_rows(d.batch);
+  const int vq = lay.view_heads(d.hq), vkv = lay.view_heads(d.hkv);
   CUtensorMap mq, mk, mv, mo;
   int st;
-  if ((st = make_head_tile_map(&mq, q, rows, d.hq, D)) != LOONG_OK) return st;
-  if ((st = make_head_tile_map(&mk, k, rows, d.hkv, D)) != LOONG_OK) return st;
-  if ((st = make_head_tile_map(&mv, v, rows, d.hkv, D)) != LOONG_OK) return st;
-  if ((st = make_head_tile_map(&mo, dout, rows, d.hq, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mq, q, rows, vq, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mk, k, rows, vkv, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mv, v, rows, vkv, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mo, dout, rows, vq, D)) != LOONG_OK) return st;
   CUtensorMap mdq;
-  if ((st = make_f32_tile_map(&mdq, dq_acc, rows, d.hq, D)) != LOONG_OK) return st;
+  if ((st = make_f32_tile_map(&mdq, dq_acc, rows, vq, D)) != LOONG_OK) return st;
   BwdArgs a;
+  a.lay = lay;
   a.batch = static_cast<int>(d.batch);
   a.S = static_cast<int>(d.seqlen);
   a.hq = d.hq;

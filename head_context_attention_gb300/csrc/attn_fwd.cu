@@ -51,6 +51,8 @@ struct FwdCfg {
 struct FwdArgs {
   int batch, S, hq, hkv, G, npairs;
   RingGeom ring;
+  Layout lay;                  // where Q, K, V, O keep (token, head)
+  int rank_begin, rank_end;    // ring ranks whose query rows this launch computes
   int t_begin, t_end;
   float scale_log2;
   __nv_bfloat16* o;
@@ -92,17 +94,22 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* drain = o_final + 1;
   volatile int* abort_flag = &abort_sh;
 
-  // ---- work item: (batch, kv head, query tile, head pair); heavy tiles first
+  // ---- work item: (batch, kv head, query tile, head pair); heavy tiles first.
+  // The query blocks of ring ranks [rank_begin, rank_end) in decreasing order:
+  // B blocks 2cp-1-c (paired placement), then A blocks c.
   const RingGeom& g = a.ring;
   int idx = blockIdx.x;
   const int hpair = idx % a.npairs;
   idx /= a.npairs;
-  const int nqt = g.nblocks * g.ntile;
+  const int nr = a.rank_end - a.rank_begin;
+  const int nqt = nr * rank_parts(g) * g.ntile;
   const int r = idx % nqt;
   idx /= nqt;
   const int kvh = idx % a.hkv;
   const int b = idx / a.hkv;
-  const int bq = g.nblocks - 1 - r / g.ntile;
+  const int jb = r / g.ntile;
+  const int bq = (g.zigzag && jb < nr) ? 2 * g.cp - 1 - a.rank_begin - jb
+                                       : a.rank_end - 1 - (g.zigzag ? jb - nr : jb);
   const int qi = g.ntile - 1 - r % g.ntile;
   const int q0 = bq * g.blk + qi * kTile;
   const int qlen = min(kTile, (bq + 1) * g.blk - q0);
@@ -148,32 +155,32 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_sh;
-  const int64_t row_base = static_cast<int64_t>(b) * a.S;
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(q_full, C::NQ * C::TILE_BYTES);
-      for (int h = 0; h < C::NQ; ++h)
+      for (int h = 0; h < C::NQ; ++h) {
+        int hc;
+        const int qr = static_cast<int>(a.lay.view_row(b, q0, h ? head1 : head0, a.hq, hc));
         for (int at = 0; at < C::ATOMS; ++at)
-          tma_load_3d(sQ + h * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, q_full, at * 64,
-                      h ? head1 : head0, static_cast<int>(row_base + q0));
+          tma_load_3d(sQ + h * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, q_full, at * 64, hc, qr);
+      }
       int jk = 0, jv = 0;
       for (int j = 0; j < n; ++j, walk.advance()) {
         const int s = j % C::NS;
         const int u = j / C::NS;
-        const int k0 = static_cast<int>(row_base + walk.k0());
+        int kvc;
+        const int k0 = static_cast<int>(a.lay.view_row(b, walk.k0(), kvh, a.hkv, kvc));
         if (j >= C::NS && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         mbar_expect_tx(&k_full[s], C::TILE_BYTES);
         for (int at = 0; at < C::ATOMS; ++at)
-          tma_load_3d(sK + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmK, &k_full[s], at * 64, kvh,
-                      k0);
+          tma_load_3d(sK + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmK, &k_full[s], at * 64, kvc, k0);
         ++jk;
         if (j >= C::NS && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         mbar_expect_tx(&v_full[s], C::TILE_BYTES);
         for (int at = 0; at < C::ATOMS; ++at)
-          tma_load_3d(sV + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmV, &v_full[s], at * 64, kvh,
-                      k0);
+          tma_load_3d(sV + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmV, &v_full[s], at * 64, kvc, k0);
         ++jv;
       }
       // Let every copy this thread issued land before the CTA can exit.
@@ -339,12 +346,12 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int head = h ? head1 : head0;
       const bool valid = row < qlen && !(h == 1 && dup);
-      const int64_t q = row_base + q0 + row;
+      const int64_t qv = a.lay.vec(b, q0 + row, head, a.hq);  // this row's d-vector in Q / O
       const float lse_p = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       float* lse_ptr = a.lse + (static_cast<int64_t>(b) * a.hq + head) * a.S + (q0 + row);
       if constexpr (!STEP) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        __nv_bfloat16* orow = a.o + (q * a.hq + head) * D;
+        __nv_bfloat16* orow = a.o + qv * D;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t ov[32];
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(320, 1)
             lse_new = mm + log2f(tot) * kLn2;
           }
         }
-        float* acc = a.o_acc + (q * a.hq + head) * D;
+        float* acc = a.o_acc + qv * D;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t ov[32];
@@ -413,14 +420,15 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool STEP>
 int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-                 float* lse, float* o_acc, cudaStream_t stream) {
+                 float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end) {
   using C = FwdCfg<D>;
-  const int64_t rows = d.batch * d.seqlen;
+  const Layout lay = layout_of(d);
+  const int64_t rows = lay.view_rows(d.batch);
   CUtensorMap mq, mk, mv;
   int st;
-  if ((st = make_head_tile_map(&mq, q, rows, d.hq, D)) != LOONG_OK) return st;
-  if ((st = make_head_tile_map(&mk, k, rows, d.hkv, D)) != LOONG_OK) return st;
-  if ((st = make_head_tile_map(&mv, v, rows, d.hkv, D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mq, q, rows, lay.view_heads(d.hq), D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mk, k, rows, lay.view_heads(d.hkv), D)) != LOONG_OK) return st;
+  if ((st = make_head_tile_map(&mv, v, rows, lay.view_heads(d.hkv), D)) != LOONG_OK) return st;
 
   FwdArgs a;
   a.batch = static_cast<int>(d.batch);
@@ -430,6 +438,9 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   a.G = d.hq / d.hkv;
   a.npairs = (a.G + 1) / 2;
   a.ring = ring_geom(d);
+  a.lay = lay;
+  a.rank_begin = rank_begin;
+  a.rank_end = rank_end;
   const float scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = scale * kLog2e;
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -441,7 +452,8 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   auto kern = ring_fwd_kernel<D, STEP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int64_t grid = d.batch * d.hkv * static_cast<int64_t>(a.ring.nblocks) * a.ring.ntile * a.npairs;
+  const int64_t grid = d.batch * d.hkv * static_cast<int64_t>(rank_end - rank_begin) * rank_parts(a.ring) *
+                       a.ring.ntile * a.npairs;
   if (grid <= 0 || grid > 0x7fffffff) return LOONG_ERR_INVALID_ARG;
   if (!STEP) {
     a.t_begin = 0;
@@ -465,14 +477,15 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
 }  // namespace
 
 int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-               float* lse, float* o_acc, cudaStream_t stream) {
+               float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end) {
   const bool step = d.mode == LOONG_MODE_STEPWISE;
+  if (rank_end < 0) rank_end = d.cp;
   if (d.head_dim == 128)
-    return step ? launch_fwd_t<128, true>(d, q, k, v, o, lse, o_acc, stream)
-                : launch_fwd_t<128, false>(d, q, k, v, o, lse, o_acc, stream);
+    return step ? launch_fwd_t<128, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end)
+                : launch_fwd_t<128, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end);
   if (d.head_dim == 64)
-    return step ? launch_fwd_t<64, true>(d, q, k, v, o, lse, o_acc, stream)
-                : launch_fwd_t<64, false>(d, q, k, v, o, lse, o_acc, stream);
+    return step ? launch_fwd_t<64, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end)
+                : launch_fwd_t<64, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end);
   return LOONG_ERR_UNSUPPORTED;
 }
 

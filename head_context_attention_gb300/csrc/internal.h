@@ -39,10 +39,13 @@ int make_head_tile_map(CUtensorMap* map, const void* base, int64_t rows, int hea
 int make_f32_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d);
 
 RingGeom ring_geom(const loong_attn_desc& d);
+// Token/head placement of the descriptor's tensors (natural or rank-major).
+Layout layout_of(const loong_attn_desc& d);
 
 // Kernel launchers (asynchronous on `stream`).
+// Query rows of ring ranks [rank_begin, rank_end) only (all of them: 0, cp).
 int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-               float* lse, float* o_acc, cudaStream_t stream);
+               float* lse, float* o_acc, cudaStream_t stream, int rank_begin = 0, int rank_end = -1);
 int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v,
                const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                float* dq_acc, float* dvec, float* dk_acc, float* dv_acc, cudaStream_t stream);

@@ -43,6 +43,60 @@ __host__ __device__ inline int rank_block(const RingGeom& g, int c, int part) {
 
 __host__ __device__ inline int rank_parts(const RingGeom& g) { return g.zigzag ? 2 : 1; }
 
+// Where a [tokens, heads, d] tensor keeps token t of sequence b, head h, seen
+// as the 3-D view [rows, view heads, d] that the TMA maps and the element
+// offsets use.
+//   natural     [B, S, H, d]: row b*S + t, view head h.
+//   rank-major  [B*cp, P, S/cp, H/P, d], the layout of every emulated rank
+//               after the Ulysses exchange ([G] "The Scalability Limits of
+//               DeepSpeed Ulysses") inside ring rank c: rank c's S/cp tokens
+//               (its blocks in part order) for head rank p's H/P heads.  Row
+//               ((b*cp + c)*P + p)*(S/cp) + u for the rank-local position u of
+//               t, view head h mod H/P.
+// A 128-token tile never crosses a block, so its rows are consecutive in
+// both layouts.
+struct Layout {
+  int rank_major;
+  int P, cp, zigzag, blk;
+  int64_t S;
+  int64_t s_rank;  // S / cp, tokens per ring rank
+
+  // rank-local position of natural token t and its ring rank c (t < S < 2^31:
+  // a 32-bit division)
+  __host__ __device__ int64_t rank_pos(int64_t t, int& c) const {
+    const int k = static_cast<int>(t) / blk;
+    const int64_t off = t - static_cast<int64_t>(k) * blk;
+    if (zigzag && k >= cp) {
+      c = 2 * cp - 1 - k;
+      return blk + off;
+    }
+    c = k;
+    return off;
+  }
+  __host__ __device__ int view_heads(int H) const { return rank_major ? H / P : H; }
+  // row of (b, t, h) in the view of a tensor with H heads, and its view head
+  __host__ __device__ int64_t view_row(int b, int64_t t, int h, int H, int& hc) const {
+    if (!rank_major) {
+      hc = h;
+      return static_cast<int64_t>(b) * S + t;
+    }
+    const int hpr = H / P;
+    const int p = h / hpr;
+    hc = h - p * hpr;
+    int c;
+    const int64_t u = rank_pos(t, c);
+    return ((static_cast<int64_t>(b) * cp + c) * P + p) * s_rank + u;
+  }
+  // index of the d-vector of (b, t, h), in units of d elements
+  __host__ __device__ int64_t vec(int b, int64_t t, int h, int H) const {
+    int hc;
+    const int64_t r = view_row(b, t, h, H, hc);
+    return r * view_heads(H) + hc;
+  }
+  // rows of the view
+  __host__ __device__ int64_t view_rows(int64_t batch) const { return batch * S * (rank_major ? P : 1); }
+};
+
 // Key tiles that the query tile (natural block bq, tile qi of that block)
 // meets over ring steps [t0, t1), in ring order: step by step, block A then
 // block B of the step's source rank, tiles in increasing position.  Blocks

@@ -326,14 +326,15 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackGeom g, int64_t 
   }
 }
 
-// Backward row statistics (see stat_row_len): for row (b, s, h) of O and dO,
+// Backward row statistics (see stat_row_len): for row (b, s, h) of O and dO
+// (rows enumerated in natural order, read where `lay` keeps them),
 // D = sum_d dO*O in fp32 and LSE*log2(e), written at the padded position of
 // token s.  16 threads per row of 128 bf16 (8 elements each), 8 for d = 64.
 template <int D>
 __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                     const float* __restrict__ lse, float* __restrict__ lse2,
                                     float* __restrict__ dstat, int64_t rows, int64_t S, int hq, int blk,
-                                    int blk_pad, int64_t stat_len) {
+                                    int blk_pad, int64_t stat_len, Layout lay) {
   constexpr int TPR = D / 8;
   const int64_t total = rows * TPR;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -344,12 +345,18 @@ __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const _
     const bool live = i < total;
     const int64_t row = live ? i / TPR : 0;
     const int part = static_cast<int>(i % TPR);
+    // row = (b*S + s)*hq + h
+    const int64_t h = row % hq;
+    const int64_t bs = row / hq;
+    const int64_t b = bs / S;
+    const int64_t s = bs - b * S;
     float acc = 0.f;
     if (live) {
-      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + part);
-      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + row * D) + part);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+      const int64_t off = lay.vec(static_cast<int>(b), s, static_cast<int>(h), hq) * D;
+      const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + off) + part);
+      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + off) + part);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 fa = __bfloat1622float2(a2[e]);
@@ -361,11 +368,6 @@ __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const _
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && part == 0) {
-      // row = (b*S + s)*hq + h
-      const int64_t h = row % hq;
-      const int64_t bs = row / hq;
-      const int64_t b = bs / S;
-      const int64_t s = bs - b * S;
       const int64_t blk_i = s / blk;
       const int64_t pos = (b * hq + h) * stat_len + blk_i * blk_pad + (s - blk_i * blk);
       dstat[pos] = acc;
@@ -470,11 +472,11 @@ int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* dou
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   const int bp = stat_block_pad(g.blk);
   if (d.head_dim == 128)
-    bwd_rowstats_kernel<128><<<grid_for(rows * 16, 256, 8), 256, 0, stream>>>(po, pd, lse, lse2, dstat, rows,
-                                                                               d.seqlen, d.hq, g.blk, bp, stat_len);
+    bwd_rowstats_kernel<128><<<grid_for(rows * 16, 256, 8), 256, 0, stream>>>(
+        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d));
   else if (d.head_dim == 64)
-    bwd_rowstats_kernel<64><<<grid_for(rows * 8, 256, 8), 256, 0, stream>>>(po, pd, lse, lse2, dstat, rows,
-                                                                             d.seqlen, d.hq, g.blk, bp, stat_len);
+    bwd_rowstats_kernel<64><<<grid_for(rows * 8, 256, 8), 256, 0, stream>>>(
+        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d));
   else
     return LOONG_ERR_UNSUPPORTED;
   return check_launch();

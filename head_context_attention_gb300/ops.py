@@ -23,9 +23,11 @@ LOONG_ERR_CUDA = -4
 LOONG_ERR_DEVICE_TIMEOUT = -5
 PLACEMENT_CONTIGUOUS, PLACEMENT_ZIGZAG = 0, 1
 MODE_STEPWISE, MODE_FUSED = 0, 1
+LAYOUT_NATURAL, LAYOUT_RANK_MAJOR = 0, 1
 
 EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loong_attn_check",
-           "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_bwd",
+           "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_fwd_ranks",
+           "loong_attn_bwd",
            "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack",
            "loong_set_timing_events", "loong_get_device_status")
 NOALLOC_SCRATCH_BYTES = 32 << 20   # LOONG_NOALLOC_SCRATCH_BYTES
@@ -37,7 +39,7 @@ class LoongAttnDesc(ctypes.Structure):
                 ("hp", ctypes.c_int32), ("cp", ctypes.c_int32),
                 ("ring_inner", ctypes.c_int32), ("ring_outer", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("placement", ctypes.c_int32), ("mode", ctypes.c_int32),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("layout", ctypes.c_int32)]
 
 
 class LoongError(RuntimeError):
@@ -71,6 +73,7 @@ def lib():
         L.loong_attn_workspace_size.argtypes = [D, ctypes.c_int]
         L.loong_ring_schedule.argtypes = [I32, I32, ctypes.POINTER(ctypes.c_int32)]
         L.loong_attn_fwd.argtypes = [D, P, P, P, P, P, P, SZ, P]
+        L.loong_attn_fwd_ranks.argtypes = [D, I32, I32, P, P, P, P, P, P]
         L.loong_attn_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.loong_attn_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P]
         L.loong_lse_merge.argtypes = [I64, I32, I32, P, P, P, P, ctypes.c_int, P]
@@ -98,10 +101,10 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_desc(w, mode=MODE_FUSED, scale=0.0):
+def make_desc(w, mode=MODE_FUSED, scale=0.0, layout=LAYOUT_NATURAL):
     """Descriptor for a ``inputs.Workload`` (or anything with the same fields)."""
     return LoongAttnDesc(w.batch, w.seqlen, w.hq, w.hkv, w.head_dim, w.hp, w.cp, w.ring_inner,
-                         w.ring_outer, 1, w.placement, mode, scale)
+                         w.ring_outer, 1, w.placement, mode, scale, layout)
 
 
 # ------------------------------------------------------------------ C entry points
@@ -124,6 +127,12 @@ def loong_attn_fwd(desc, q, k, v, o, lse, ws=None, stream=None):
     nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     return _check("loong_attn_fwd", lib().loong_attn_fwd(
         ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), nbytes,
+        _stream(stream)))
+
+
+def loong_attn_fwd_ranks(desc, rank_begin, rank_end, q, k, v, o, lse, stream=None):
+    return _check("loong_attn_fwd_ranks", lib().loong_attn_fwd_ranks(
+        ctypes.byref(desc), rank_begin, rank_end, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
         _stream(stream)))
 
 
@@ -167,9 +176,10 @@ def workspace(desc, pass_, device="cuda"):
     return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def attn_fwd(w, q, k, v, mode=MODE_FUSED, stream=None):
-    """Allocate O and LSE with torch, run loong_attn_fwd, return (o, lse)."""
-    desc = make_desc(w, mode)
+def attn_fwd(w, q, k, v, mode=MODE_FUSED, stream=None, layout=LAYOUT_NATURAL):
+    """Allocate O and LSE with torch, run loong_attn_fwd, return (o, lse).
+    With LAYOUT_RANK_MAJOR, q/k/v (and o) are headctx_pack outputs."""
+    desc = make_desc(w, mode, layout=layout)
     _check("loong_attn_check", loong_attn_check(desc))
     o = torch.empty_like(q)
     lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=q.device)
@@ -177,9 +187,9 @@ def attn_fwd(w, q, k, v, mode=MODE_FUSED, stream=None):
     return o, lse
 
 
-def attn_bwd(w, q, k, v, o, lse, do, mode=MODE_FUSED, stream=None):
-    """Allocate dQ/dK/dV with torch, run loong_attn_bwd, return them."""
-    desc = make_desc(w, mode)
+def attn_bwd(w, q, k, v, o, lse, do, mode=MODE_FUSED, stream=None, layout=LAYOUT_NATURAL):
+    """Allocate dQ/dK/dV with torch, run loong_attn_bwd, return them (in the layout of q, k)."""
+    desc = make_desc(w, mode, layout=layout)
     _check("loong_attn_check", loong_attn_check(desc))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, workspace(desc, 1, q.device), stream)

@@ -17,9 +17,15 @@
  *     cached device query, a loaded tensor-map encoder and one device error
  *     word, and synchronises only in loong_get_device_status.
  *   - All work is enqueued asynchronously on `stream` (0 = legacy default).
- *   - Tensors are contiguous.  Q, O, dO, dQ: bf16 [B, S, Hq, d]; K, V, dK, dV:
- *     bf16 [B, S, Hkv, d], natural token order; LSE: fp32 [B, Hq, S], natural
- *     log of the softmax denominator of the scaled logits.
+ *   - Tensors are contiguous.  In the NATURAL layout Q, O, dO, dQ are bf16
+ *     [B, S, Hq, d] and K, V, dK, dV bf16 [B, S, Hkv, d], natural token order.
+ *     In the RANK_MAJOR layout (descriptor field `layout`) they are
+ *     [B*cp, hp, S/cp, H/hp, d] with H = Hq or Hkv: ring rank c's S/cp tokens
+ *     (its blocks in part order, as the placement assigns them) for head rank
+ *     p's H/hp heads, which is what loong_headctx_pack (direction 0, gather 1
+ *     for ZIGZAG, 2 for CONTIGUOUS) produces from the natural layout.  LSE is
+ *     fp32 [B, Hq, S] in natural token order in both: the natural log of the
+ *     softmax denominator of the scaled logits.
  *   - Base pointers must be 16-byte aligned.
  *   - Return value: LOONG_OK (0) or a negative loong_status.  No exception
  *     crosses the ABI; no call aborts the process or traps the GPU.
@@ -57,6 +63,7 @@ typedef enum {
 
 enum { LOONG_PLACEMENT_CONTIGUOUS = 0, LOONG_PLACEMENT_ZIGZAG = 1 };
 enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1 };
+enum { LOONG_LAYOUT_NATURAL = 0, LOONG_LAYOUT_RANK_MAJOR = 1 };
 
 /*
  * Problem descriptor.  Follows the problem statement of [G] "1. 2D Mesh
@@ -85,6 +92,10 @@ enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1 };
  *                     fp32 accumulator by log-sum-exp.
  *   softmax_scale     <= 0 selects 1/sqrt(head_dim) ([G] "Step 3",
  *                     forward_local_attention).
+ *   layout            LOONG_LAYOUT_NATURAL or LOONG_LAYOUT_RANK_MAJOR (the
+ *                     per-rank layout after the Ulysses exchange, [G] "The
+ *                     Scalability Limits of DeepSpeed Ulysses"; see above).
+ *                     RANK_MAJOR needs batch * seqlen * hp < 2^31.
  */
 typedef struct {
   int64_t batch, seqlen;
@@ -94,6 +105,7 @@ typedef struct {
   int32_t placement;
   int32_t mode;
   float softmax_scale;
+  int32_t layout;
 } loong_attn_desc;
 
 /* Library version, (major << 16) | minor. */
@@ -114,11 +126,11 @@ LOONG_API int loong_attn_check(const loong_attn_desc* desc);
 /*
  * Device workspace, in bytes, that loong_attn_fwd (pass 0) or loong_attn_bwd
  * (pass 1) needs for `desc`; 0 for an invalid descriptor.  Host-only.
- *   fwd, FUSED: 0.  fwd, STEPWISE: fp32 O accumulator [B,S,Hq,d].
- *   bwd: fp32 dQ accumulator [B,S,Hq,d] + fp32 row statistics (LSE*log2 e
+ *   fwd, FUSED: 0.  fwd, STEPWISE: fp32 O accumulator, B*S*Hq*d values.
+ *   bwd: fp32 dQ accumulator (B*S*Hq*d) + fp32 row statistics (LSE*log2 e
  *        and D = rowsum(dO*O)), 2 x B x Hq x (nblocks*roundup(blk,4) + 128)
  *        values, with nblocks = 2cp (ZIGZAG) or cp and blk = S/nblocks,
- *        + fp32 dK, dV accumulators [B,S,Hkv,d] each.
+ *        + fp32 dK, dV accumulators, B*S*Hkv*d values each.
  *   Each part starts on a 256-byte boundary.
  */
 LOONG_API size_t loong_attn_workspace_size(const loong_attn_desc* desc, int pass);
@@ -139,7 +151,7 @@ LOONG_API int loong_ring_schedule(int32_t ring_inner, int32_t ring_outer, int32_
  * result by log-sum-exp.  The result equals causal attention over the whole
  * sequence up to rounding.
  *   q, k, v   inputs (layouts above), read only.
- *   o         bf16 output [B,S,Hq,d].
+ *   o         bf16 output, the layout of q.
  *   lse       fp32 output [B,Hq,S].
  *   ws        device workspace of at least loong_attn_workspace_size(desc,0)
  *             bytes (may be NULL when that size is 0).
@@ -148,14 +160,28 @@ LOONG_API int loong_attn_fwd(const loong_attn_desc* desc, const void* q, const v
                    void* o, float* lse, void* ws, size_t ws_bytes, loong_stream_t stream);
 
 /*
+ * loong_attn_fwd restricted to the query rows of ring ranks
+ * [rank_begin, rank_end) (all heads, all sequences of the batch): the work of
+ * those emulated ranks alone, so that one rank's share of the ring pass can be
+ * timed ([G] section 2 gives every rank the same work under paired blocks).
+ * Rows of other ranks in o and lse are left untouched; the rows written equal
+ * those of loong_attn_fwd bit for bit.  FUSED mode only (STEPWISE returns
+ * LOONG_ERR_UNSUPPORTED); no workspace.  0 <= rank_begin < rank_end <= cp.
+ */
+LOONG_API int loong_attn_fwd_ranks(const loong_attn_desc* desc, int32_t rank_begin, int32_t rank_end,
+                                   const void* q, const void* k, const void* v, void* o, float* lse,
+                                   loong_stream_t stream);
+
+/*
  * Backward of loong_attn_fwd: the exact gradient of causal softmax attention
  * (the pages give no backward; this is the plain chain rule through softmax).
  * Over the same schedule: P = exp(s - LSE), dV += P^T dO, dP = dO V^T,
  * dS = P * (dP - D) with D = rowsum(dO * O), dQ += scale dS K,
  * dK += scale dS^T Q; dK and dV sum over the query heads of a kv group.
  *   o, lse    the outputs of loong_attn_fwd for the same inputs.
- *   dout      bf16 dO [B,S,Hq,d].
- *   dq        bf16 [B,S,Hq,d]; dk, dv bf16 [B,S,Hkv,d]; written, not added to.
+ *   dout      bf16 dO, the layout of q.
+ *   dq        bf16, the layout of q; dk, dv bf16, the layout of k; written,
+ *             not added to.
  *   ws        at least loong_attn_workspace_size(desc,1) bytes.
  */
 LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const void* k, const void* v,

@@ -62,6 +62,8 @@ def _desc(**kw):
     ("placement", 7, ops.LOONG_ERR_INVALID_ARG),
     ("mode", 3, ops.LOONG_ERR_INVALID_ARG),
     ("batch", 0, ops.LOONG_ERR_INVALID_ARG),
+    ("layout", 2, ops.LOONG_ERR_INVALID_ARG),
+    ("layout", ops.LAYOUT_RANK_MAJOR, ops.LOONG_OK),
 ])
 def test_descriptor_validation(loong_lib, field, value, status):
     assert ops.loong_attn_check(_desc()) == ops.LOONG_OK
@@ -109,3 +111,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         ops.lib()
+
+
+def test_rank_major_view_rows_must_fit_int32(loong_lib):
+    # the rank-major view has B*S*hp rows; its TMA row coordinate is 32-bit
+    d = _desc(batch=2048, layout=ops.LAYOUT_RANK_MAJOR)      # 2048 * 131072 * 8 rows
+    assert ops.loong_attn_check(d) == ops.LOONG_ERR_UNSUPPORTED
+    d = _desc(batch=2, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_check(d) == ops.LOONG_OK
+
+
+def test_fwd_ranks_validation_before_any_cuda_call(loong_lib):
+    L = ops.lib()
+    d = _desc()
+    args = (None,) * 6
+    for lo, hi in ((-1, 2), (3, 3), (4, 2), (0, d.cp + 1)):
+        assert L.loong_attn_fwd_ranks(ctypes.byref(d), lo, hi, *args) == ops.LOONG_ERR_INVALID_ARG
+    assert L.loong_attn_fwd_ranks(ctypes.byref(d), 0, 1, *args) == ops.LOONG_ERR_INVALID_ARG  # null tensors
+    step = _desc(mode=ops.MODE_STEPWISE)
+    assert L.loong_attn_fwd_ranks(ctypes.byref(step), 0, 1, *args) == ops.LOONG_ERR_UNSUPPORTED

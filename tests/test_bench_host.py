@@ -79,10 +79,23 @@ def test_recorded_traffic_follows_kernel_sources(monkeypatch):
     """The committed ncu DRAM record is reported only for the kernel sources it
     was taken on; any other source hash gives null traffic."""
     rec = json.load(open(os.path.join(ROOT, "profiles", "roofline_traffic.json")))
-    ent = rec["kernels"]["ring_bwd_kernel"]["llama3-8b-s128k"]
+    ent = rec["kernels"]["ring_bwd_kernel"]["llama3-8b-s128k"]["rank-major"]
     assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"]
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha256"])
     assert bench.recorded_traffic("ring_bwd_kernel", "llama3-8b-s128k") == ent["dram_bytes_per_launch"]
     assert bench.recorded_traffic("ring_bwd_kernel", "no-such-workload") is None
+    assert bench.recorded_traffic("ring_bwd_kernel", "llama3-8b-s128k", "no-such-layout") is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 64)
     assert bench.recorded_traffic("ring_bwd_kernel", "llama3-8b-s128k") is None
+
+
+@pytest.mark.parametrize("placement", [0, 1])
+@pytest.mark.parametrize("seqlen,cp", [(1024, 4), (131072, 16), (96, 3)])
+def test_rank_pairs_match_the_oracle_schedule(placement, seqlen, cp):
+    """The bench's per-rank work count (closed form) equals the oracle's count
+    over the rank's token positions."""
+    from head_context_attention_gb300 import inputs
+    from oracle import schedule
+    w = inputs.WORKLOADS["tiny-gqa-s1k"].with_(seqlen=seqlen, cp=cp, ring_inner=cp, ring_outer=1)
+    for c in range(cp):
+        assert bench.rank_pairs(w, placement, c) == schedule.pair_work(seqlen, cp, c, placement)
