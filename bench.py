@@ -43,7 +43,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    p.add_argument("--mode", default="fused", choices=["fused", "stepwise"])
+    p.add_argument("--mode", default="fused", choices=["fused", "stepwise", "stepwise-copy"],
+                   help="stepwise-copy: one launch per ring step, K/V delivered by device-to-device copies "
+                        "on a side stream (rank-major layout)")
     p.add_argument("--layout", default="rank-major", choices=["rank-major", "natural"],
                    help="rank-major: the step repacks in and out around the ring kernels (2D attention)")
     p.add_argument("--no-e2e", action="store_true")
@@ -125,6 +127,40 @@ def time_lse_merge(w, o, lse, stream, dev, reps=5):
     del o_parts, lse_parts, o_out, lse_out
     return {"ms": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "bytes": nbytes, "parts": 2,
             "rows": rows}
+
+
+# ------------------------------------------------------------------ exchange copies
+def time_exchange_alone(w, path, stream, dev, reps=3):
+    """The device-to-device copies of one STEPWISE_COPY pass on their own: for
+    ring steps 1..cp-1, every rank's incoming K and V chunk into a receive
+    buffer, the same transfers the library issues on its side stream."""
+    import torch
+
+    from head_context_attention_gb300 import ops
+
+    sched = ops.loong_ring_schedule(w.ring_inner, w.ring_outer)
+    k, v = path.kt["k"], path.kt["v"]
+    rk, rv = torch.empty_like(k), torch.empty_like(v)
+
+    def copies():
+        for t in range(1, w.cp):
+            for b in range(w.batch):
+                for c in range(w.cp):
+                    j = sched[t][c]
+                    rk[b * w.cp + c].copy_(k[b * w.cp + j], non_blocking=True)
+                    rv[b * w.cp + c].copy_(v[b * w.cp + j], non_blocking=True)
+
+    copies()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        copies()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    nbytes = (w.cp - 1) * 2 * k.numel() * k.element_size()
+    return {"bytes_per_pass": nbytes, "copy_ms_alone": round(ms, 3), "gbs": round(2 * nbytes / (ms * 1e-3) / 1e9, 1),
+            "note": "copies of one pass timed alone; in the step they run on a side stream beside the kernels"}
 
 
 # ------------------------------------------------------------------ per-rank work
@@ -413,7 +449,7 @@ def run_gpu(args, w, rank, local, world, pg):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    mode = ops.MODE_FUSED if args.mode == "fused" else ops.MODE_STEPWISE
+    mode = {"fused": ops.MODE_FUSED, "stepwise": ops.MODE_STEPWISE, "stepwise-copy": ops.MODE_STEPWISE_COPY}[args.mode]
     stream = torch.cuda.current_stream(dev)
     path = TwoDPath(w, mode, args.layout, dev, stream)
     x = inputs.make_inputs(w, device=dev, with_do=True)
@@ -471,6 +507,7 @@ def run_gpu(args, w, rank, local, world, pg):
     ms_total = max_over_ranks(pg, ms_total, dev)
     merge_rec = time_lse_merge(w, path.out["o"], path.lse, stream, dev)
     per_rank = time_per_rank(w, x, stream, dev) if args.per_rank else None
+    exchange = time_exchange_alone(w, path, stream, dev) if mode == ops.MODE_STEPWISE_COPY else None
     ms_step = ms_total / args.steps
     f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
     b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b) if do_bwd else 0.0
@@ -526,6 +563,8 @@ def run_gpu(args, w, rank, local, world, pg):
     }
     if per_rank is not None:
         result["per_rank_fwd"] = per_rank
+    if exchange is not None:
+        result["exchange"] = exchange
     rejected = [r for r in clocks.get("reasons", []) if r in SLOWDOWN_REASONS]
     if rejected:
         result["clocks"]["rejected"] = rejected

@@ -32,6 +32,7 @@
 
 #include <cmath>
 
+#include "exchange.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -70,6 +71,7 @@ struct BwdArgs {
   int batch, S, hq, hkv, G;
   RingGeom ring;
   Layout lay;  // where Q, K, V, dO, dQ (and its accumulator), dK, dV keep (token, head)
+  int kv_held;  // K, V are receive buffers (one step per launch): read the holder rank's plane
   int t_begin, t_end;
   float scale, scale_log2;
   // Row statistics, [B*Hq][stat_len] each, block b's rows at b*blk_pad:
@@ -187,7 +189,10 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) {
       mbar_expect_tx(kv_full, 2 * C::TILE_BYTES);
       int kvc;
-      const int kr = static_cast<int>(a.lay.view_row(b, k0, kvh, a.hkv, kvc));
+      // the rank that holds this key tile's chunk at the launch's (single) step
+      const int holder = ring_dst(block_owner(g, bk), a.t_begin, g.inner, g.outer);
+      const int kr = static_cast<int>(a.kv_held ? a.lay.view_row_held(b, k0, kvh, a.hkv, holder, kvc)
+                                                : a.lay.view_row(b, k0, kvh, a.hkv, kvc));
       for (int at = 0; at < C::ATOMS; ++at) {
         tma_load_3d(sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvc, kr);
         tma_load_3d(sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvc, kr);
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(352, 1)
 template <int D, bool STEP>
 int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const void* v, const void* dout,
                  const float* stats, float* dq_acc, void* dk, void* dv, float* dk_acc,
-                 float* dv_acc, cudaStream_t stream) {
+                 float* dv_acc, cudaStream_t stream, void* kv_recv) {
   using C = BwdCfg<D>;
   const Layout lay = layout_of(d);
   const int64_t rows = lay.view_rows(d.batch);
@@ -613,6 +618,7 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   if ((st = make_f32_tile_map(&mdq, dq_acc, rows, vq, D)) != LOONG_OK) return st;
   BwdArgs a;
   a.lay = lay;
+  a.kv_held = 0;
   a.batch = static_cast<int>(d.batch);
   a.S = static_cast<int>(d.seqlen);
   a.hq = d.hq;
@@ -646,6 +652,30 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
     record_stop(stream);
     return check_launch();
   }
+  if (d.mode == LOONG_MODE_STEPWISE_COPY) {
+    // receive buffers K0, K1, V0, V1, each the size of K (exchange.h); dK, dV
+    // are accumulated at the owner's rows, so only K and V travel
+    const size_t kv_bytes = static_cast<size_t>(rows) * vkv * D * 2;
+    uint8_t* rb = static_cast<uint8_t*>(kv_recv);
+    void* const rk[2] = {rb, rb + kv_bytes};
+    void* const rv[2] = {rb + 2 * kv_bytes, rb + 3 * kv_bytes};
+    CUtensorMap mkr[2], mvr[2];
+    for (int i = 0; i < 2; ++i) {
+      if ((st = make_head_tile_map(&mkr[i], rk[i], rows, vkv, D)) != LOONG_OK) return st;
+      if ((st = make_head_tile_map(&mvr[i], rv[i], rows, vkv, D)) != LOONG_OK) return st;
+    }
+    record_start(stream);
+    st = run_exchanged_steps(d, k, v, rk, rv, stream, [&](int t, int buf) {
+      a.t_begin = t;
+      a.t_end = t + 1;
+      a.kv_held = buf >= 0;
+      kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(
+          mq, buf >= 0 ? mkr[buf] : mk, buf >= 0 ? mvr[buf] : mv, mo, mdq, a);
+      return check_launch();
+    });
+    record_stop(stream);
+    return st;
+  }
   record_start(stream);
   for (int t = t_first; t < t_last; ++t) {
     a.t_begin = t;
@@ -661,10 +691,10 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
 
 int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, const void* o,
                const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dq_acc, float* dvec,
-               float* dk_acc, float* dv_acc, cudaStream_t stream) {
+               float* dk_acc, float* dv_acc, cudaStream_t stream, void* kv_recv) {
   const int64_t q_elems = d.batch * d.seqlen * d.hq * d.head_dim;
   const int64_t kv_elems = d.batch * d.seqlen * d.hkv * d.head_dim;
-  const bool step = d.mode == LOONG_MODE_STEPWISE;
+  const bool step = d.mode != LOONG_MODE_FUSED;
   int st;
   cudaError_t e = cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -673,11 +703,11 @@ int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const voi
     return cuda_fail(e);
   if ((st = launch_bwd_rowstats(d, o, dout, lse, dvec, stream)) != LOONG_OK) return st;
   if (d.head_dim == 128)
-    st = step ? launch_bwd_t<128, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream)
-              : launch_bwd_t<128, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream);
+    st = step ? launch_bwd_t<128, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream, kv_recv)
+              : launch_bwd_t<128, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream, kv_recv);
   else if (d.head_dim == 64)
-    st = step ? launch_bwd_t<64, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream)
-              : launch_bwd_t<64, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream);
+    st = step ? launch_bwd_t<64, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream, kv_recv)
+              : launch_bwd_t<64, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream, kv_recv);
   else
     return LOONG_ERR_UNSUPPORTED;
   if (st != LOONG_OK) return st;

@@ -26,6 +26,7 @@
 
 #include <cmath>
 
+#include "exchange.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -53,6 +54,7 @@ struct FwdArgs {
   RingGeom ring;
   Layout lay;                  // where Q, K, V, O keep (token, head)
   int rank_begin, rank_end;    // ring ranks whose query rows this launch computes
+  int kv_held;                 // K, V are receive buffers: read the query rank's plane
   int t_begin, t_end;
   float scale_log2;
   __nv_bfloat16* o;
@@ -167,11 +169,13 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_3d(sQ + h * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, q_full, at * 64, hc, qr);
       }
       int jk = 0, jv = 0;
+      const int c_q = block_owner(g, bq);  // the query tile's ring rank
       for (int j = 0; j < n; ++j, walk.advance()) {
         const int s = j % C::NS;
         const int u = j / C::NS;
         int kvc;
-        const int k0 = static_cast<int>(a.lay.view_row(b, walk.k0(), kvh, a.hkv, kvc));
+        const int k0 = static_cast<int>(a.kv_held ? a.lay.view_row_held(b, walk.k0(), kvh, a.hkv, c_q, kvc)
+                                                  : a.lay.view_row(b, walk.k0(), kvh, a.hkv, kvc));
         if (j >= C::NS && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         mbar_expect_tx(&k_full[s], C::TILE_BYTES);
         for (int at = 0; at < C::ATOMS; ++at)
@@ -420,7 +424,7 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool STEP>
 int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-                 float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end) {
+                 float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end, void* kv_recv) {
   using C = FwdCfg<D>;
   const Layout lay = layout_of(d);
   const int64_t rows = lay.view_rows(d.batch);
@@ -441,6 +445,7 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   a.lay = lay;
   a.rank_begin = rank_begin;
   a.rank_end = rank_end;
+  a.kv_held = 0;
   const float scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = scale * kLog2e;
   a.o = static_cast<__nv_bfloat16*>(o);
@@ -463,6 +468,29 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
     record_stop(stream);
     return check_launch();
   }
+  if (d.mode == LOONG_MODE_STEPWISE_COPY) {
+    // receive buffers K0, K1, V0, V1, each the size of K
+    const size_t kv_bytes = static_cast<size_t>(rows) * lay.view_heads(d.hkv) * D * 2;
+    uint8_t* rb = static_cast<uint8_t*>(kv_recv);
+    void* const rk[2] = {rb, rb + kv_bytes};
+    void* const rv[2] = {rb + 2 * kv_bytes, rb + 3 * kv_bytes};
+    CUtensorMap mkr[2], mvr[2];
+    for (int i = 0; i < 2; ++i) {
+      if ((st = make_head_tile_map(&mkr[i], rk[i], rows, lay.view_heads(d.hkv), D)) != LOONG_OK) return st;
+      if ((st = make_head_tile_map(&mvr[i], rv[i], rows, lay.view_heads(d.hkv), D)) != LOONG_OK) return st;
+    }
+    record_start(stream);
+    st = run_exchanged_steps(d, k, v, rk, rv, stream, [&](int t, int buf) {
+      a.t_begin = t;
+      a.t_end = t + 1;
+      a.kv_held = buf >= 0;
+      kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, buf >= 0 ? mkr[buf] : mk,
+                                                                               buf >= 0 ? mvr[buf] : mv, a);
+      return check_launch();
+    });
+    record_stop(stream);
+    return st;
+  }
   record_start(stream);
   for (int t = 0; t < d.cp; ++t) {
     a.t_begin = t;
@@ -477,15 +505,15 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
 }  // namespace
 
 int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-               float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end) {
-  const bool step = d.mode == LOONG_MODE_STEPWISE;
+               float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end, void* kv_recv) {
+  const bool step = d.mode != LOONG_MODE_FUSED;
   if (rank_end < 0) rank_end = d.cp;
   if (d.head_dim == 128)
-    return step ? launch_fwd_t<128, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end)
-                : launch_fwd_t<128, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end);
+    return step ? launch_fwd_t<128, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv)
+                : launch_fwd_t<128, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv);
   if (d.head_dim == 64)
-    return step ? launch_fwd_t<64, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end)
-                : launch_fwd_t<64, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end);
+    return step ? launch_fwd_t<64, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv)
+                : launch_fwd_t<64, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv);
   return LOONG_ERR_UNSUPPORTED;
 }
 

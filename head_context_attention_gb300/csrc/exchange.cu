@@ -1,0 +1,60 @@
+// exchange.cu -- side stream, events and copies of the ring exchange stand-in
+// (exchange.h).
+#include <mutex>
+
+#include "exchange.h"
+
+namespace loong {
+
+namespace {
+
+struct ExchangeSlot {
+  std::once_flag once;
+  Exchange ex;
+  cudaError_t status = cudaSuccess;
+};
+ExchangeSlot g_ex[64];
+
+}  // namespace
+
+Exchange* exchange_for_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= 64) return nullptr;
+  ExchangeSlot* s = &g_ex[dev];
+  std::call_once(s->once, [s]() {
+    cudaError_t r = cudaStreamCreateWithFlags(&s->ex.side, cudaStreamNonBlocking);
+    if (r == cudaSuccess) r = cudaEventCreateWithFlags(&s->ex.entry, cudaEventDisableTiming);
+    for (int i = 0; i < 2 && r == cudaSuccess; ++i) {
+      r = cudaEventCreateWithFlags(&s->ex.ready[i], cudaEventDisableTiming);
+      if (r == cudaSuccess) r = cudaEventCreateWithFlags(&s->ex.freed[i], cudaEventDisableTiming);
+    }
+    s->status = r;
+  });
+  if (s->status != cudaSuccess) {
+    cuda_fail(s->status);
+    return nullptr;
+  }
+  return &s->ex;
+}
+
+int exchange_copies(const loong_attn_desc& d, int t, const void* src, void* recv, size_t chunk_bytes,
+                    cudaStream_t side) {
+  const auto* s = static_cast<const uint8_t*>(src);
+  auto* r = static_cast<uint8_t*>(recv);
+  for (int64_t b = 0; b < d.batch; ++b)
+    for (int c = 0; c < d.cp; ++c) {
+      const int j = ring_src(c, t, d.ring_inner, d.ring_outer);
+      const size_t to = static_cast<size_t>(b * d.cp + c) * chunk_bytes;
+      const size_t from = static_cast<size_t>(b * d.cp + j) * chunk_bytes;
+      cudaError_t e = cudaMemcpyAsync(r + to, s + from, chunk_bytes, cudaMemcpyDeviceToDevice, side);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+  return LOONG_OK;
+}
+
+}  // namespace loong

@@ -44,11 +44,14 @@ Layout layout_of(const loong_attn_desc& d);
 
 // Kernel launchers (asynchronous on `stream`).
 // Query rows of ring ranks [rank_begin, rank_end) only (all of them: 0, cp).
+// STEPWISE_COPY: kv_recv holds the K0, K1, V0, V1 receive buffers (exchange.h).
 int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-               float* lse, float* o_acc, cudaStream_t stream, int rank_begin = 0, int rank_end = -1);
+               float* lse, float* o_acc, cudaStream_t stream, int rank_begin = 0, int rank_end = -1,
+               void* kv_recv = nullptr);
 int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v,
                const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
-               float* dq_acc, float* dvec, float* dk_acc, float* dv_acc, cudaStream_t stream);
+               float* dq_acc, float* dvec, float* dk_acc, float* dv_acc, cudaStream_t stream,
+               void* kv_recv = nullptr);
 
 int launch_fill_f32(float* p, int64_t n, float value, cudaStream_t stream);
 int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);

@@ -87,6 +87,16 @@ struct Layout {
     const int64_t u = rank_pos(t, c);
     return ((static_cast<int64_t>(b) * cp + c) * P + p) * s_rank + u;
   }
+  // rank-major only: the row of (b, t, h) in ring rank `holder`'s plane, at
+  // t's rank-local position (where a rank keeps the chunk it has received)
+  __host__ __device__ int64_t view_row_held(int b, int64_t t, int h, int H, int holder, int& hc) const {
+    const int hpr = H / P;
+    const int p = h / hpr;
+    hc = h - p * hpr;
+    int c;
+    const int64_t u = rank_pos(t, c);
+    return ((static_cast<int64_t>(b) * cp + holder) * P + p) * s_rank + u;
+  }
   // index of the d-vector of (b, t, h), in units of d elements
   __host__ __device__ int64_t vec(int b, int64_t t, int h, int H) const {
     int hc;

@@ -22,7 +22,7 @@ LOONG_ERR_UNSUPPORTED = -3
 LOONG_ERR_CUDA = -4
 LOONG_ERR_DEVICE_TIMEOUT = -5
 PLACEMENT_CONTIGUOUS, PLACEMENT_ZIGZAG = 0, 1
-MODE_STEPWISE, MODE_FUSED = 0, 1
+MODE_STEPWISE, MODE_FUSED, MODE_STEPWISE_COPY = 0, 1, 2
 LAYOUT_NATURAL, LAYOUT_RANK_MAJOR = 0, 1
 
 EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loong_attn_check",

@@ -62,7 +62,7 @@ typedef enum {
 } loong_status;
 
 enum { LOONG_PLACEMENT_CONTIGUOUS = 0, LOONG_PLACEMENT_ZIGZAG = 1 };
-enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1 };
+enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1, LOONG_MODE_STEPWISE_COPY = 2 };
 enum { LOONG_LAYOUT_NATURAL = 0, LOONG_LAYOUT_RANK_MAJOR = 1 };
 
 /*
@@ -89,7 +89,18 @@ enum { LOONG_LAYOUT_NATURAL = 0, LOONG_LAYOUT_RANK_MAJOR = 1 };
  *   mode              LOONG_MODE_FUSED: one launch walks all ring steps and
  *                     keeps the running softmax on chip; STEPWISE: one launch
  *                     per ring step, each merging its partial result into an
- *                     fp32 accumulator by log-sum-exp.
+ *                     fp32 accumulator by log-sum-exp.  STEPWISE_COPY
+ *                     (RANK_MAJOR layout only): STEPWISE with the ring's K/V
+ *                     exchange made real ([G] "3. Double-Ring Asynchronous
+ *                     Communication Pipeline"): before step t >= 1 every ring
+ *                     rank's incoming chunk is copied (cudaMemcpyAsync, device
+ *                     to device) into its receive buffer on a side stream the
+ *                     library owns, double-buffered so that the copies of step
+ *                     t overlap the kernel of step t-1, and the kernels read
+ *                     K/V from the receive buffers.  dK, dV are added at their
+ *                     owner's rows (their return trip is not copied).  The
+ *                     side stream and its events are one per device: calls in
+ *                     this mode on one device must not overlap.
  *   softmax_scale     <= 0 selects 1/sqrt(head_dim) ([G] "Step 3",
  *                     forward_local_attention).
  *   layout            LOONG_LAYOUT_NATURAL or LOONG_LAYOUT_RANK_MAJOR (the
@@ -127,6 +138,8 @@ LOONG_API int loong_attn_check(const loong_attn_desc* desc);
  * Device workspace, in bytes, that loong_attn_fwd (pass 0) or loong_attn_bwd
  * (pass 1) needs for `desc`; 0 for an invalid descriptor.  Host-only.
  *   fwd, FUSED: 0.  fwd, STEPWISE: fp32 O accumulator, B*S*Hq*d values.
+ *   STEPWISE_COPY adds, to both passes, four bf16 receive buffers of
+ *        B*S*Hkv*d values each (K and V, two of each).
  *   bwd: fp32 dQ accumulator (B*S*Hq*d) + fp32 row statistics (LSE*log2 e
  *        and D = rowsum(dO*O)), 2 x B x Hq x (nblocks*roundup(blk,4) + 128)
  *        values, with nblocks = 2cp (ZIGZAG) or cp and blk = S/nblocks,

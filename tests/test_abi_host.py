@@ -63,6 +63,7 @@ def _desc(**kw):
     ("mode", 3, ops.LOONG_ERR_INVALID_ARG),
     ("batch", 0, ops.LOONG_ERR_INVALID_ARG),
     ("layout", 2, ops.LOONG_ERR_INVALID_ARG),
+    ("mode", ops.MODE_STEPWISE_COPY, ops.LOONG_ERR_UNSUPPORTED),   # needs the rank-major layout
     ("layout", ops.LAYOUT_RANK_MAJOR, ops.LOONG_OK),
 ])
 def test_descriptor_validation(loong_lib, field, value, status):
@@ -130,3 +131,13 @@ def test_fwd_ranks_validation_before_any_cuda_call(loong_lib):
     assert L.loong_attn_fwd_ranks(ctypes.byref(d), 0, 1, *args) == ops.LOONG_ERR_INVALID_ARG  # null tensors
     step = _desc(mode=ops.MODE_STEPWISE)
     assert L.loong_attn_fwd_ranks(ctypes.byref(step), 0, 1, *args) == ops.LOONG_ERR_UNSUPPORTED
+
+
+def test_stepwise_copy_mode_needs_rank_major_and_receive_buffers(loong_lib):
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    d = ops.make_desc(w, ops.MODE_STEPWISE_COPY, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_check(d) == ops.LOONG_OK
+    step = ops.make_desc(w, ops.MODE_STEPWISE, layout=ops.LAYOUT_RANK_MAJOR)
+    recv = 4 * ((w.seqlen * w.hkv * w.head_dim * 2 + 255) // 256 * 256)
+    for p in (0, 1):
+        assert ops.loong_attn_workspace_size(d, p) == ops.loong_attn_workspace_size(step, p) + recv
