@@ -209,3 +209,47 @@ def test_d_rounding_bound_covers_rounded_o_and_is_tight_enough():
     rk, rv = attention.attention_backward_keys(q, k, v, do, keys, 0, d_from_bf16_o=True)
     assert np.all(np.abs(rk - ek) <= kb + 1e-12)
     np.testing.assert_array_equal(rv, ev)
+
+
+# ---- non-causal attention ([G] "Step 3" carries an is_causal flag)
+def test_noncausal_forward_matches_torch_sdpa_float64():
+    rng = np.random.default_rng(21)
+    q, k, v, _ = _rand(rng, 29, 8, 2, 16)
+    o, lse = attention.attention_forward(q, k, v, causal=False)
+    tq = torch.from_numpy(q).permute(1, 0, 2)[None]
+    tk = torch.from_numpy(k).permute(1, 0, 2)[None].repeat_interleave(4, dim=1)
+    tv = torch.from_numpy(v).permute(1, 0, 2)[None].repeat_interleave(4, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=False)
+    np.testing.assert_allclose(o, ref[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+    s = torch.einsum("hqd,hkd->hqk", tq[0], tk[0]) / math.sqrt(16)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_noncausal_output_ignores_key_order():
+    """Without the mask a query attends to a set of keys: permuting the K/V
+    rows together leaves every output unchanged (a mask bug would not)."""
+    rng = np.random.default_rng(22)
+    q, k, v, _ = _rand(rng, 17, 4, 2, 8)
+    perm = rng.permutation(17)
+    o1, l1 = attention.attention_forward(q, k, v, causal=False)
+    o2, l2 = attention.attention_forward(q, k[perm], v[perm], causal=False)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+    oc, _ = attention.attention_forward(q, k, v, causal=True)
+    assert np.abs(oc[0] - o1[0]).max() > 1e-3   # row 0 sees all keys here, only key 0 when causal
+
+
+def test_noncausal_backward_matches_torch_autograd_float64():
+    rng = np.random.default_rng(23)
+    q, k, v, do = _rand(rng, 19, 4, 2, 8)
+    dq, dk, dv, *_ = attention.attention_backward(q, k, v, do, causal=False)
+    tq = torch.from_numpy(q).requires_grad_()
+    tk = torch.from_numpy(k).requires_grad_()
+    tv = torch.from_numpy(v).requires_grad_()
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq.permute(1, 0, 2)[None], tk.permute(1, 0, 2)[None].repeat_interleave(2, dim=1),
+        tv.permute(1, 0, 2)[None].repeat_interleave(2, dim=1), is_causal=False)
+    ref[0].permute(1, 0, 2).backward(torch.from_numpy(do))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
