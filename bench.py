@@ -56,6 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--seqlen", type=int, default=0,
                    help="override S (a smaller case of the same shape, e.g. for profiler captures)")
     p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
+    p.add_argument("--non-causal", action="store_true",
+                   help="every query sees every key (FLOPs counted over all S^2 pairs)")
     return p.parse_args(argv)
 
 
@@ -545,7 +547,7 @@ def run_gpu(args, w, rank, local, world, pg):
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "hq": w.hq, "hkv": w.hkv,
                    "head_dim": w.head_dim, "hp": w.hp, "cp": w.cp, "ring_inner": w.ring_inner,
                    "ring_outer": w.ring_outer, "placement": "zigzag" if w.placement == 1 else "contiguous",
-                   "mode": args.mode, "layout": args.layout,
+                   "mode": args.mode, "layout": args.layout, "causal": w.causal,
                    "step": ("repack Q,K,V,dO -> ring fwd + bwd on the rank-major layout -> repack O,dQ,dK,dV"
                             if path.rank_major else "ring fwd + bwd on the natural layout"),
                    "parallelism": f"replicas x{world} (each rank: all hp x cp ranks emulated)",
@@ -650,6 +652,8 @@ def main(argv=None):
     if args.seqlen:
         w = w.with_(seqlen=args.seqlen, name=f"{w.name}@S={args.seqlen}")
     w = w.with_(backward=not args.fwd_only)
+    if args.non_causal:
+        w = w.with_(causal=False, name=f"{w.name}@non-causal")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
 

@@ -153,6 +153,7 @@ RingGeom ring_geom(const loong_attn_desc& d) {
   g.cp = d.cp;
   g.inner = d.ring_inner;
   g.outer = d.ring_outer;
+  g.causal = d.causal;
   g.zigzag = d.placement == LOONG_PLACEMENT_ZIGZAG;
   g.nblocks = g.zigzag ? 2 * d.cp : d.cp;
   g.blk = static_cast<int>(d.seqlen / g.nblocks);
@@ -215,7 +216,7 @@ int loong_attn_check(const loong_attn_desc* d) {
   if (d->batch * d->seqlen > 0x7fffffffLL || view_rows > 0x7fffffffLL) return LOONG_ERR_UNSUPPORTED;
   if (!std::isfinite(d->softmax_scale)) return LOONG_ERR_INVALID_ARG;
   if (!is_pow2_ok_hd(d->head_dim)) return LOONG_ERR_UNSUPPORTED;
-  if (d->causal != 1) return LOONG_ERR_UNSUPPORTED;
+  if (d->causal != 0 && d->causal != 1) return LOONG_ERR_INVALID_ARG;
   // the exchange copies whole per-rank chunks: contiguous only in the rank-major layout
   if (d->mode == LOONG_MODE_STEPWISE_COPY && d->layout != LOONG_LAYOUT_RANK_MAJOR) return LOONG_ERR_UNSUPPORTED;
   return LOONG_OK;

@@ -68,6 +68,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // Of every 8 consecutive score columns, this many take their exponential on
 // the FMA pipe (exp2_fma) instead of the MUFU unit.
+template <int D>
 constexpr int kFmaExpPer8 = 0;
 
 template <int D, bool STEP>
@@ -290,17 +291,16 @@ __global__ void __launch_bounds__(320, 1)
           for (int i = 0; i < 32; ++i)
             if (cb * 32 + i > lim) sr[cb][i] = __float_as_uint(-INFINITY);
       }
-      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+      // row maximum, two new columns per (three-input) max
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[cb][i]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[cb][i + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[cb][i + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[cb][i + 3]));
+          mx0 = fmax3(mx0, __uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1]));
+          mx1 = fmax3(mx1, __uint_as_float(sr[cb][i + 2]), __uint_as_float(sr[cb][i + 3]));
         }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_tile = fmaxf(mx0, mx1) * sl2;
       const float m_new = fmaxf(m_run, m_tile);
       const bool rescale = j > 0 && m_new > m_run + kRescaleThreshold;
       if (j == 0) m_run = m_new;
@@ -322,21 +322,23 @@ __global__ void __launch_bounds__(320, 1)
         if (rescale) m_run = m_new;
       }
       const float ref = m_run == -INFINITY ? 0.f : m_run;
-      float l0 = 0.f, l1 = 0.f;
+      // column pairs on the paired fp32 pipe: x = s*scale*log2e - m, and the
+      // two running sums (each half rounds as the scalar operation would)
+      const float2 sl2v = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
+      float2 lsum = make_float2(0.f, 0.f);
       uint32_t pk[2][32];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float x0 = fmaf(__uint_as_float(sr[cb][i]), sl2, -ref);
-          const float x1 = fmaf(__uint_as_float(sr[cb][i + 1]), sl2, -ref);
-          const float p0 = (i & 7) < kFmaExpPer8 ? exp2_fma(x0) : fast_exp2(x0);
-          const float p1 = ((i + 1) & 7) < kFmaExpPer8 ? exp2_fma(x1) : fast_exp2(x1);
-          l0 += p0;
-          l1 += p1;
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1])),
+                                      sl2v, nref);
+          const float p0 = (i & 7) < kFmaExpPer8<D> ? exp2_fma(x.x) : fast_exp2(x.x);
+          const float p1 = ((i + 1) & 7) < kFmaExpPer8<D> ? exp2_fma(x.y) : fast_exp2(x.y);
+          lsum = __fadd2_rn(lsum, make_float2(p0, p1));
           pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
         }
-      l_run += l0 + l1;
+      l_run += lsum.x + lsum.y;
       tmem_st32(tS, pk[0]);
       tmem_st32(tS + 32, pk[1]);
       tmem_wait_st();

@@ -19,6 +19,7 @@ constexpr int kTile = 128;  // rows of a query tile and of a key tile
 
 struct RingGeom {
   int cp, inner, outer;
+  int causal;   // 1: query i sees keys j <= i; 0: every key
   int zigzag;   // 1 paired blocks, 0 contiguous
   int blk;      // tokens per block
   int nblocks;  // blocks per sequence: 2*cp or cp
@@ -109,9 +110,9 @@ struct Layout {
 
 // Key tiles that the query tile (natural block bq, tile qi of that block)
 // meets over ring steps [t0, t1), in ring order: step by step, block A then
-// block B of the step's source rank, tiles in increasing position.  Blocks
-// that lie wholly after bq are skipped; the block bq itself is visited up to
-// the diagonal tile qi.
+// block B of the step's source rank, tiles in increasing position.  Causal:
+// blocks that lie wholly after bq are skipped and the block bq itself is
+// visited up to the diagonal tile qi.  Non-causal: every tile of every block.
 struct KvWalk {
   RingGeom g;
   int c, bq, qi, t, t1, part, kt, kt_n, bk;
@@ -131,7 +132,7 @@ struct KvWalk {
     while (t < t1) {
       const int j = ring_src(c, t, g.inner, g.outer);
       bk = rank_block(g, j, part);
-      kt_n = bk < bq ? g.ntile : (bk == bq ? qi + 1 : 0);
+      kt_n = (!g.causal || bk < bq) ? g.ntile : (bk == bq ? qi + 1 : 0);
       if (kt < kt_n) return;
       kt = 0;
       if (++part == rank_parts(g)) {
@@ -146,7 +147,7 @@ struct KvWalk {
     const int e = (bk + 1) * g.blk - k0();
     return e < kTile ? e : kTile;
   }
-  __host__ __device__ bool diag() const { return bk == bq && kt == qi; }
+  __host__ __device__ bool diag() const { return g.causal && bk == bq && kt == qi; }
   __host__ __device__ void advance() {
     ++kt;
     settle();
@@ -160,7 +161,7 @@ struct KvWalk {
     while (tt < t1) {
       const int j = ring_src(c, tt, g.inner, g.outer);
       const int b = rank_block(g, j, pp);
-      const int m = b < bq ? g.ntile : (b == bq ? qi + 1 : 0);
+      const int m = (!g.causal || b < bq) ? g.ntile : (b == bq ? qi + 1 : 0);
       if (m > first) n += m - first;
       first = 0;
       if (++pp == rank_parts(g)) {
@@ -209,7 +210,7 @@ struct QWalk {
     while (t < t1) {
       const int c = ring_dst(j, t, g.inner, g.outer);
       bq = rank_block(g, c, part);
-      qlo = bk < bq ? 0 : (bk == bq ? kt : g.ntile);
+      qlo = (!g.causal || bk < bq) ? 0 : (bk == bq ? kt : g.ntile);
       len = g.ntile - qlo;
       if (len > 0) {
         k = 0;
@@ -248,14 +249,14 @@ struct QWalk {
     const int e = (bq + 1) * g.blk - q0();
     return e < kTile ? e : kTile;
   }
-  __host__ __device__ bool diag() const { return bq == bk && qi == kt; }
+  __host__ __device__ bool diag() const { return g.causal && bq == bk && qi == kt; }
   __host__ __device__ int count() const {
     int n = 0;
     for (int tt = t; tt < t1; ++tt) {
       const int c = ring_dst(j, tt, g.inner, g.outer);
       for (int pp = 0; pp < rank_parts(g); ++pp) {
         const int b = rank_block(g, c, pp);
-        if (bk < b) n += g.ntile;
+        if (!g.causal || bk < b) n += g.ntile;
         else if (bk == b) n += g.ntile - kt;
       }
     }

@@ -34,6 +34,7 @@ class Workload:
     peaky_keys: float = 0.0
     batch: int = 1
     placement: int = 1          # 1 paired blocks (zigzag), 0 contiguous
+    causal: bool = True
     note: str = field(default="", compare=False)
 
     def with_(self, **kw):
@@ -41,8 +42,9 @@ class Workload:
 
     @property
     def fwd_flops(self):
-        """Causal forward FLOPs: 2 GEMMs x 2 flops x the S^2/2 causal half."""
-        return 2 * self.batch * self.seqlen * self.seqlen * self.hq * self.head_dim
+        """Forward FLOPs: 2 GEMMs x 2 flops over the S^2/2 causal half (all S^2
+        pairs when not causal)."""
+        return (2 if self.causal else 4) * self.batch * self.seqlen * self.seqlen * self.hq * self.head_dim
 
     @property
     def flops(self):
@@ -58,6 +60,8 @@ WORKLOADS = {
                                    False, note="Llama-3-8B attention layer, forward"),
     "llama3-8b-s128k": Workload("llama3-8b-s128k", 131072, 32, 8, 128, 8, 16, 8, 2, True,
                                 note="Llama-3-8B attention layer, fwd+bwd"),
+    "gqa-d64-s128k": Workload("gqa-d64-s128k", 131072, 32, 8, 64, 8, 16, 8, 2, True,
+                              note="the same mesh and heads with head dimension 64, fwd+bwd"),
     "llama3-70b-s256k": Workload("llama3-70b-s256k", 262144, 64, 8, 128, 8, 32, 8, 4, True,
                                  repack=True,
                                  note="Llama-3-70B attention layer, fwd+bwd + Q/K/V repack"),

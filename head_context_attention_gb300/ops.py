@@ -104,7 +104,7 @@ def _stream(stream):
 def make_desc(w, mode=MODE_FUSED, scale=0.0, layout=LAYOUT_NATURAL):
     """Descriptor for a ``inputs.Workload`` (or anything with the same fields)."""
     return LoongAttnDesc(w.batch, w.seqlen, w.hq, w.hkv, w.head_dim, w.hp, w.cp, w.ring_inner,
-                         w.ring_outer, 1, w.placement, mode, scale, layout)
+                         w.ring_outer, 1 if getattr(w, "causal", True) else 0, w.placement, mode, scale, layout)
 
 
 # ------------------------------------------------------------------ C entry points

@@ -80,9 +80,9 @@ enum { LOONG_LAYOUT_NATURAL = 0, LOONG_LAYOUT_RANK_MAJOR = 1 };
  *   ring_inner/outer  double-ring shape, inner * outer == cp.  At step
  *                     t = o*inner + i ring rank c holds the K/V of rank
  *                     ((c/inner - o) mod outer)*inner + ((c%inner - i) mod inner).
- *   causal            must be 1 (query i sees key j only for j <= i, [G] "The
+ *   causal            1: query i sees key j only for j <= i ([G] "The
  *                     Communication Overhead and Causal Imbalance of Ring
- *                     Attention").
+ *                     Attention"); 0: every key ([G] "Step 3", is_causal off).
  *   placement         LOONG_PLACEMENT_ZIGZAG: ring rank r owns blocks r and
  *                     2cp-1-r of length S/(2cp); CONTIGUOUS: block r of length
  *                     S/cp.  The block length must be a multiple of hp.

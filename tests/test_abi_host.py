@@ -58,7 +58,8 @@ def _desc(**kw):
     ("ring_inner", 4, ops.LOONG_ERR_INVALID_ARG),   # inner * outer != cp
     ("seqlen", 131072 + 32, ops.LOONG_ERR_INVALID_ARG),  # S % (2 cp)
     ("head_dim", 96, ops.LOONG_ERR_UNSUPPORTED),
-    ("causal", 0, ops.LOONG_ERR_UNSUPPORTED),
+    ("causal", 0, ops.LOONG_OK),
+    ("causal", 2, ops.LOONG_ERR_INVALID_ARG),
     ("placement", 7, ops.LOONG_ERR_INVALID_ARG),
     ("mode", 3, ops.LOONG_ERR_INVALID_ARG),
     ("batch", 0, ops.LOONG_ERR_INVALID_ARG),
