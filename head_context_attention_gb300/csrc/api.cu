@@ -345,6 +345,13 @@ int loong_set_timing_events(void* start_event, void* stop_event) {
   return LOONG_OK;
 }
 
+int loong_selftest_wait_timeout(uint32_t limit_us, loong_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return LOONG_ERR_INVALID_ARG;
+  int st = device_ready();
+  if (st != LOONG_OK) return st;
+  return launch_wait_probe(limit_us, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int loong_get_device_status(loong_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);

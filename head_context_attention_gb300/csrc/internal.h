@@ -54,6 +54,8 @@ int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const voi
                void* kv_recv = nullptr);
 
 int launch_fill_f32(float* p, int64_t n, float value, cudaStream_t stream);
+// One CTA whose bounded mbarrier wait has nothing to wait for (selftest.cu).
+int launch_wait_probe(uint32_t limit_us, cudaStream_t stream);
 int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
 int launch_lse_merge(int64_t rows, int d, int n_parts, const float* o_parts,
                      const float* lse_parts, void* o_out, float* lse_out, int out_bf16,

@@ -64,21 +64,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false when
-// the CTA's abort flag is raised or the wait exceeds kWaitLimitNs; in the
-// latter case the abort flag and the device error word are set.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* err) {
+// the CTA's abort flag is raised or the wait exceeds limit_ns; in the latter
+// case the abort flag and the device error word are set.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned* err, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(err, kErrWaitTimeout);
       return false;
     }
   }
+}
+
+// The kernels' wait: mbar_wait_for with kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned* err) {
+  return mbar_wait_for(bar, parity, abort_flag, err, kWaitLimitNs);
 }
 
 // Bounded wait used only on the way out of a kernel (draining copies in

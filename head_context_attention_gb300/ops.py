@@ -29,7 +29,7 @@ EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loo
            "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_fwd_ranks",
            "loong_attn_bwd",
            "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack",
-           "loong_set_timing_events", "loong_get_device_status")
+           "loong_set_timing_events", "loong_get_device_status", "loong_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 32 << 20   # LOONG_NOALLOC_SCRATCH_BYTES
 
 
@@ -81,6 +81,7 @@ def lib():
                                          P, P, P]
         L.loong_set_timing_events.argtypes = [P, P]
         L.loong_get_device_status.argtypes = [P]
+        L.loong_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
         _lib = L
     return _lib
 
@@ -168,6 +169,10 @@ def loong_set_timing_events(start=None, stop=None):
 
 def loong_get_device_status(stream=None):
     return lib().loong_get_device_status(_stream(stream))
+
+
+def loong_selftest_wait_timeout(limit_us, stream=None):
+    return lib().loong_selftest_wait_timeout(limit_us, _stream(stream))
 
 
 # ------------------------------------------------------------------ conveniences

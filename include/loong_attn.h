@@ -14,8 +14,9 @@
  *   - Pointers named q, k, v, o, dout, dq, dk, dv, lse, ws, in, out, o_parts,
  *     lse_parts, o_out, lse_out are DEVICE pointers owned by the caller.  The
  *     library allocates no device memory, keeps no state between calls except a
- *     cached device query, a loaded tensor-map encoder and one device error
- *     word, and synchronises only in loong_get_device_status.
+ *     cached device query, a loaded tensor-map encoder, one device error word
+ *     and (STEPWISE_COPY) one side stream with its events per device, and
+ *     synchronises only in loong_get_device_status.
  *   - All work is enqueued asynchronously on `stream` (0 = legacy default).
  *   - Tensors are contiguous.  In the NATURAL layout Q, O, dO, dQ are bf16
  *     [B, S, Hq, d] and K, V, dK, dV bf16 [B, S, Hkv, d], natural token order.
@@ -286,6 +287,18 @@ LOONG_API int loong_set_timing_events(void* start_event, void* stop_event);
  * LOONG_OK otherwise.
  */
 LOONG_API int loong_get_device_status(loong_stream_t stream);
+
+/*
+ * Self-test of the bounded-wait path (no counterpart on the pages): launches
+ * one CTA on `stream` whose mbarrier wait, the same code every kernel's waits
+ * use, has nothing to wait for.  It gives up after limit_us microseconds
+ * (1 .. 1000000), raises the CTA's abort flag, sets the device error word and
+ * returns, so the next loong_get_device_status reports
+ * LOONG_ERR_DEVICE_TIMEOUT and clears the word; the context stays usable.
+ * Returns LOONG_ERR_INVALID_ARG for a limit out of range (before any CUDA
+ * call), else the launch status.
+ */
+LOONG_API int loong_selftest_wait_timeout(uint32_t limit_us, loong_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -142,3 +142,9 @@ def test_stepwise_copy_mode_needs_rank_major_and_receive_buffers(loong_lib):
     recv = 4 * ((w.seqlen * w.hkv * w.head_dim * 2 + 255) // 256 * 256)
     for p in (0, 1):
         assert ops.loong_attn_workspace_size(d, p) == ops.loong_attn_workspace_size(step, p) + recv
+
+
+def test_selftest_wait_limit_validated_before_any_cuda_call(loong_lib):
+    L = ops.lib()
+    for bad in (0, 1000001):
+        assert L.loong_selftest_wait_timeout(bad, None) == ops.LOONG_ERR_INVALID_ARG
