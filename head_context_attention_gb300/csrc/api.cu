@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace loong {
 
@@ -190,6 +191,7 @@ const char* loong_status_string(int status) {
     case LOONG_ERR_UNSUPPORTED: return "unsupported configuration or device";
     case LOONG_ERR_CUDA: return "CUDA error";
     case LOONG_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case LOONG_ERR_DEVICE_CHECK: return "device address check failed";
     default: return "unknown status";
   }
 }
@@ -363,7 +365,7 @@ int loong_get_device_status(loong_stream_t stream) {
   if (word) {
     e = cudaMemset(p, 0, sizeof(unsigned));
     if (e != cudaSuccess) return cuda_fail(e);
-    return LOONG_ERR_DEVICE_TIMEOUT;
+    return (word & (kErrBounds | kErrSmemAlign)) ? LOONG_ERR_DEVICE_CHECK : LOONG_ERR_DEVICE_TIMEOUT;
   }
   return LOONG_OK;
 }

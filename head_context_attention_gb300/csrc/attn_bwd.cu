@@ -191,8 +191,11 @@ __global__ void __launch_bounds__(352, 1)
       int kvc;
       // the rank that holds this key tile's chunk at the launch's (single) step
       const int holder = ring_dst(block_owner(g, bk), a.t_begin, g.inner, g.outer);
-      const int kr = static_cast<int>(a.kv_held ? a.lay.view_row_held(b, k0, kvh, a.hkv, holder, kvc)
-                                                : a.lay.view_row(b, k0, kvh, a.hkv, kvc));
+      const int64_t kr64 = a.kv_held ? a.lay.view_row_held(b, k0, kvh, a.hkv, holder, kvc)
+                                     : a.lay.view_row(b, k0, kvh, a.hkv, kvc);
+      // checked build: tiles start inside their tensors (TMA fills rows past the end with zeros)
+      in_bounds(kr64 >= 0 && kr64 < a.lay.view_rows(a.batch) && kvc >= 0 && kvc < a.lay.view_heads(a.hkv), a.err);
+      const int kr = static_cast<int>(kr64);
       for (int at = 0; at < C::ATOMS; ++at) {
         tma_load_3d(sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvc, kr);
         tma_load_3d(sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvc, kr);
@@ -204,7 +207,9 @@ __global__ void __launch_bounds__(352, 1)
         // coordinates first, off the wait's critical path
         const int head = kvh * a.G + walk.head;
         int hc;
-        const int qrow = static_cast<int>(a.lay.view_row(b, walk.q0(), head, a.hq, hc));
+        const int64_t qrow64 = a.lay.view_row(b, walk.q0(), head, a.hq, hc);
+        in_bounds(qrow64 >= 0 && qrow64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
+        const int qrow = static_cast<int>(qrow64);
         if (i >= C::NS && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         mbar_expect_tx(&q_full[s], 2 * C::TILE_BYTES + C::STAT_BYTES);
         for (int at = 0; at < C::ATOMS; ++at) {
@@ -212,8 +217,14 @@ __global__ void __launch_bounds__(352, 1)
           tma_load_3d(sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, hc, qrow);
         }
         // this tile's row statistics: 16-byte aligned and in bounds by construction
-        const int64_t srow = (static_cast<int64_t>(b) * a.hq + head) * a.stat_len + walk.bq * a.blk_pad +
-                             walk.qi * kTile;
+        int64_t srow = (static_cast<int64_t>(b) * a.hq + head) * a.stat_len + walk.bq * a.blk_pad +
+                       walk.qi * kTile;
+        // checked build: a plain bulk copy must stay inside the statistics rows
+        // (else it reads row 0 instead, keeping the barrier's byte count)
+        if (!in_bounds(srow >= 0 && srow % 4 == 0 &&
+                           srow + kTile <= (static_cast<int64_t>(b) * a.hq + head + 1) * a.stat_len,
+                       a.err))
+          srow = 0;
         bulk_load(sStat + s * (2 * kTile), a.lse2 + srow, kTile * 4, &q_full[s]);
         bulk_load(sStat + s * (2 * kTile) + kTile, a.dstat + srow, kTile * 4, &q_full[s]);
         ++issued;
@@ -313,14 +324,18 @@ __global__ void __launch_bounds__(352, 1)
         const int s = i % C::NS;
         const int head = kvh * a.G + walk.head;
         int hc;
-        const int qrow = static_cast<int>(a.lay.view_row(b, walk.q0(), head, a.hq, hc));
+        const int64_t qrow64 = a.lay.view_row(b, walk.q0(), head, a.hq, hc);
+        // checked build: a reduction never starts outside the accumulator (skipped if it would)
+        const bool red_ok =
+            in_bounds(qrow64 >= 0 && qrow64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
+        const int qrow = static_cast<int>(qrow64);
         if (!mbar_wait(staged, i & 1, abort_flag, a.err)) break;
 #pragma unroll
         for (int box = 0; box < C::DQ_BOXES; ++box) {
           const uint8_t* base = box < C::BOXES_PER_STAGE
                                     ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
                                     : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
-          tma_reduce_add_3d(&tmDQ, base, box * 32, hc, qrow);
+          if (red_ok) tma_reduce_add_3d(&tmDQ, base, box * 32, hc, qrow);
         }
         bulk_commit_group();
         bulk_wait_read_all();
@@ -335,7 +350,11 @@ __global__ void __launch_bounds__(352, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row in the pass, query row in the dQ drain
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool key_ok = row < klen;
+    // checked build: this key row's dK / dV / accumulator rows lie inside their tensors
+    const bool key_ok = row < klen && in_bounds(a.lay.vec(b, k0 + row, kvh, a.hkv) >= 0 &&
+                                                    a.lay.vec(b, k0 + row, kvh, a.hkv) <
+                                                        static_cast<int64_t>(a.batch) * a.S * a.hkv,
+                                                a.err);
     const int64_t krow = a.lay.vec(b, k0 + row, kvh, a.hkv);  // this key row's d-vector in K / dK / dV
     // group 0 owns dV, group 1 owns dK (keys on lanes)
     const uint32_t acc_col = grp == 0 ? C::RV : C::RK;

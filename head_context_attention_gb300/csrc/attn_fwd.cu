@@ -165,7 +165,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_expect_tx(q_full, C::NQ * C::TILE_BYTES);
       for (int h = 0; h < C::NQ; ++h) {
         int hc;
-        const int qr = static_cast<int>(a.lay.view_row(b, q0, h ? head1 : head0, a.hq, hc));
+        const int64_t qr64 = a.lay.view_row(b, q0, h ? head1 : head0, a.hq, hc);
+        // checked build: the tile starts inside the tensor (TMA fills rows past its end with zeros)
+        in_bounds(qr64 >= 0 && qr64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
+        const int qr = static_cast<int>(qr64);
         for (int at = 0; at < C::ATOMS; ++at)
           tma_load_3d(sQ + h * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, q_full, at * 64, hc, qr);
       }
@@ -175,8 +178,10 @@ __global__ void __launch_bounds__(320, 1)
         const int s = j % C::NS;
         const int u = j / C::NS;
         int kvc;
-        const int k0 = static_cast<int>(a.kv_held ? a.lay.view_row_held(b, walk.k0(), kvh, a.hkv, c_q, kvc)
-                                                  : a.lay.view_row(b, walk.k0(), kvh, a.hkv, kvc));
+        const int64_t k064 = a.kv_held ? a.lay.view_row_held(b, walk.k0(), kvh, a.hkv, c_q, kvc)
+                                       : a.lay.view_row(b, walk.k0(), kvh, a.hkv, kvc);
+        in_bounds(k064 >= 0 && k064 < a.lay.view_rows(a.batch) && kvc >= 0 && kvc < a.lay.view_heads(a.hkv), a.err);
+        const int k0 = static_cast<int>(k064);
         if (j >= C::NS && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
         mbar_expect_tx(&k_full[s], C::TILE_BYTES);
         for (int at = 0; at < C::ATOMS; ++at)
@@ -351,10 +356,15 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) {
       tc_fence_after();
       const int head = h ? head1 : head0;
-      const bool valid = row < qlen && !(h == 1 && dup);
       const int64_t qv = a.lay.vec(b, q0 + row, head, a.hq);  // this row's d-vector in Q / O
+      const int64_t lse_i = (static_cast<int64_t>(b) * a.hq + head) * a.S + (q0 + row);
+      // checked build: the row's O, accumulator and LSE entries lie inside their tensors
+      const bool valid = row < qlen && !(h == 1 && dup) &&
+                         in_bounds(qv >= 0 && qv < static_cast<int64_t>(a.batch) * a.S * a.hq && lse_i >= 0 &&
+                                       lse_i < static_cast<int64_t>(a.batch) * a.hq * a.S,
+                                   a.err);
       const float lse_p = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-      float* lse_ptr = a.lse + (static_cast<int64_t>(b) * a.hq + head) * a.S + (q0 + row);
+      float* lse_ptr = a.lse + lse_i;
       if constexpr (!STEP) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
         __nv_bfloat16* orow = a.o + qv * D;

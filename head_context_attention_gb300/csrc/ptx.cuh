@@ -14,7 +14,26 @@ namespace loong {
 enum : unsigned {
   kErrWaitTimeout = 1u,
   kErrSmemAlign = 2u,  // dynamic shared memory not 1024-byte aligned: kernel did nothing
+  kErrBounds = 4u,     // checked build: an address check failed, the access was skipped
 };
+
+#ifdef LOONG_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// Checked build: record a failed address check in the error word and return
+// false, so the caller skips the access.  Other builds: always true (the
+// condition is not evaluated into any code).
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned* err) {
+  if constexpr (kChecked) {
+    if (!ok) atomicOr(err, kErrBounds);
+    return ok;
+  } else {
+    return true;
+  }
+}
 
 // A bounded wait gives up after this many nanoseconds of global time.  Every
 // legitimate wait in these kernels lasts microseconds.

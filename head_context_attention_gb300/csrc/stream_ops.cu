@@ -221,6 +221,8 @@ struct PackGeom {
   int W;                  // 16-byte vectors per output row
   int tile_rows;          // output rows per tile
   FastDiv fW, fRv;        // division by W and by Hp * vpr
+  int64_t in_vecs, out_vecs;  // sizes of the two tensors in 16-byte vectors (checked build)
+  unsigned* err;
 };
 
 // Natural token of rank-local position u of ring rank c.
@@ -314,13 +316,18 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PackGeom g, int64_t 
             const uint32_t p = fdiv(w, g.fRv);
             off = p * plane + (w - p * g.fRv.d);
           }
-          v[k] = __ldg(in + src_row[r] + off);
+          const int64_t from = src_row[r] + off;
+          // checked build: both ends of the copy lie inside their tensors
+          if (in_bounds(from >= 0 && from < g.in_vecs && (row0 + r) * g.W + w < g.out_vecs, g.err))
+            v[k] = __ldg(in + from);
+          else
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
 #pragma unroll
       for (int k = 0; k < U; ++k) {
         const int j = j0 + k * kPackThreads;
-        if (j < nvec) dst[j] = v[k];
+        if (j < nvec && in_bounds(row0 * g.W + j < g.out_vecs, g.err)) dst[j] = v[k];
       }
     }
   }
@@ -334,7 +341,7 @@ template <int D>
 __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                     const float* __restrict__ lse, float* __restrict__ lse2,
                                     float* __restrict__ dstat, int64_t rows, int64_t S, int hq, int blk,
-                                    int blk_pad, int64_t stat_len, Layout lay) {
+                                    int blk_pad, int64_t stat_len, Layout lay, unsigned* err) {
   constexpr int TPR = D / 8;
   const int64_t total = rows * TPR;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -351,8 +358,10 @@ __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const _
     const int64_t b = bs / S;
     const int64_t s = bs - b * S;
     float acc = 0.f;
-    if (live) {
-      const int64_t off = lay.vec(static_cast<int>(b), s, static_cast<int>(h), hq) * D;
+    const int64_t off = lay.vec(static_cast<int>(b), s, static_cast<int>(h), hq) * D;
+    // checked build: the row's O / dO vectors lie inside the tensors
+    const bool row_ok = !live || in_bounds(off >= 0 && off + D <= rows * D, err);
+    if (live && row_ok) {
       const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + off) + part);
       const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + off) + part);
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
@@ -370,8 +379,10 @@ __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const _
     if (live && part == 0) {
       const int64_t blk_i = s / blk;
       const int64_t pos = (b * hq + h) * stat_len + blk_i * blk_pad + (s - blk_i * blk);
-      dstat[pos] = acc;
-      lse2[pos] = lse[(b * hq + h) * S + s] * kLog2e;
+      if (row_ok && in_bounds(pos >= 0 && pos < (b * hq + h + 1) * stat_len, err)) {
+        dstat[pos] = acc;
+        lse2[pos] = lse[(b * hq + h) * S + s] * kLog2e;
+      }
     }
   }
 }
@@ -450,6 +461,9 @@ int launch_headctx_pack(int64_t batch, int cp, int P, int64_t s_local, int heads
   g.tile_rows = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kPackMaxRows, 2048 / w)));
   g.fW = make_fastdiv(static_cast<uint32_t>(g.W));
   g.fRv = make_fastdiv(static_cast<uint32_t>(g.Hp * g.vpr));
+  g.in_vecs = g.out_vecs = batch * g.seqlen * heads * g.vpr;  // both directions move the whole tensor
+  g.err = device_error_word();
+  if (!g.err) return LOONG_ERR_CUDA;
   const int64_t ntiles = (total_rows + g.tile_rows - 1) / g.tile_rows;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(num_sms()) * 8));
   if (direction == 0)
@@ -471,12 +485,14 @@ int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* dou
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   const int bp = stat_block_pad(g.blk);
+  unsigned* err = device_error_word();
+  if (!err) return LOONG_ERR_CUDA;
   if (d.head_dim == 128)
     bwd_rowstats_kernel<128><<<grid_for(rows * 16, 256, 8), 256, 0, stream>>>(
-        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d));
+        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
   else if (d.head_dim == 64)
     bwd_rowstats_kernel<64><<<grid_for(rows * 8, 256, 8), 256, 0, stream>>>(
-        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d));
+        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
   else
     return LOONG_ERR_UNSUPPORTED;
   return check_launch();

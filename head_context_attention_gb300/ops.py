@@ -14,6 +14,8 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libloong_attn.so")
+# the same library with device address checks (LOONG_CHECKED)
+CHECKED_LIB_PATH = os.path.join(_PKG, "libloong_attn_checked.so")
 
 LOONG_OK = 0
 LOONG_ERR_INVALID_ARG = -1
@@ -21,6 +23,7 @@ LOONG_ERR_WORKSPACE = -2
 LOONG_ERR_UNSUPPORTED = -3
 LOONG_ERR_CUDA = -4
 LOONG_ERR_DEVICE_TIMEOUT = -5
+LOONG_ERR_DEVICE_CHECK = -6
 PLACEMENT_CONTIGUOUS, PLACEMENT_ZIGZAG = 0, 1
 MODE_STEPWISE, MODE_FUSED, MODE_STEPWISE_COPY = 0, 1, 2
 LAYOUT_NATURAL, LAYOUT_RANK_MAJOR = 0, 1

@@ -54,12 +54,17 @@ typedef enum {
   LOONG_OK = 0,
   LOONG_ERR_INVALID_ARG = -1,     /* null pointer, bad size or divisibility   */
   LOONG_ERR_WORKSPACE = -2,       /* ws_bytes smaller than the workspace size */
-  LOONG_ERR_UNSUPPORTED = -3,     /* valid but not built: head_dim, non-causal,
-                                     device is not compute capability 10.3    */
+  LOONG_ERR_UNSUPPORTED = -3,     /* valid but not built: head_dim, a mode /
+                                     layout pairing, device is not compute
+                                     capability 10.3                          */
   LOONG_ERR_CUDA = -4,            /* a CUDA call failed; see loong_last_cuda_error */
-  LOONG_ERR_DEVICE_TIMEOUT = -5   /* a kernel's bounded wait expired; the
+  LOONG_ERR_DEVICE_TIMEOUT = -5,  /* a kernel's bounded wait expired; the
                                      kernel stopped early and its outputs are
                                      undefined                                  */
+  LOONG_ERR_DEVICE_CHECK = -6     /* libloong_attn_checked.so: a device
+                                     address check failed and the access was
+                                     skipped (or shared memory was misaligned);
+                                     outputs are undefined                      */
 } loong_status;
 
 enum { LOONG_PLACEMENT_CONTIGUOUS = 0, LOONG_PLACEMENT_ZIGZAG = 1 };
@@ -282,9 +287,10 @@ LOONG_API int loong_set_timing_events(void* start_event, void* stop_event);
 
 /*
  * Synchronise `stream` and report device-side failures of earlier calls:
- * LOONG_ERR_DEVICE_TIMEOUT if a kernel's bounded wait expired (the error word
- * is then cleared), LOONG_ERR_CUDA if the stream reports a CUDA error,
- * LOONG_OK otherwise.
+ * LOONG_ERR_DEVICE_CHECK if an address check of the checked build failed or a
+ * kernel found its shared memory misaligned, else LOONG_ERR_DEVICE_TIMEOUT if
+ * a kernel's bounded wait expired (the error word is then cleared),
+ * LOONG_ERR_CUDA if the stream reports a CUDA error, LOONG_OK otherwise.
  */
 LOONG_API int loong_get_device_status(loong_stream_t stream);
 
