@@ -249,6 +249,7 @@ int loong_ring_schedule(int32_t inner, int32_t outer, int32_t* src) {
 
 int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, void* o,
                    float* lse, void* ws, size_t ws_bytes, loong_stream_t stream_) {
+  NvtxRange range("loong_attn_fwd");
   int st = loong_attn_check(d);
   if (st != LOONG_OK) return st;
   if (!q || !k || !v || !o || !lse) return LOONG_ERR_INVALID_ARG;
@@ -272,6 +273,7 @@ int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const
 
 int loong_attn_fwd_ranks(const loong_attn_desc* d, int32_t rank_begin, int32_t rank_end, const void* q,
                          const void* k, const void* v, void* o, float* lse, loong_stream_t stream_) {
+  NvtxRange range("loong_attn_fwd_ranks");
   int st = loong_attn_check(d);
   if (st != LOONG_OK) return st;
   if (d->mode != LOONG_MODE_FUSED) return LOONG_ERR_UNSUPPORTED;
@@ -286,6 +288,7 @@ int loong_attn_fwd_ranks(const loong_attn_desc* d, int32_t rank_begin, int32_t r
 int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, const void* o,
                    const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                    size_t ws_bytes, loong_stream_t stream_) {
+  NvtxRange range("loong_attn_bwd");
   int st = loong_attn_check(d);
   if (st != LOONG_OK) return st;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return LOONG_ERR_INVALID_ARG;
@@ -311,6 +314,7 @@ int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const
 
 int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts, const float* o_parts, const float* lse_parts,
                     void* o_out, float* lse_out, int out_bf16, loong_stream_t stream) {
+  NvtxRange range("loong_lse_merge");
   if (rows < 0 || d < 1 || d > 1024 || d % 4 || n_parts < 1 || n_parts > 64) return LOONG_ERR_INVALID_ARG;
   if (out_bf16 != 0 && out_bf16 != 1) return LOONG_ERR_INVALID_ARG;
   if (rows == 0) return LOONG_OK;
@@ -326,6 +330,7 @@ int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts, const float* o_par
 
 int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s_local, int32_t heads, int32_t d,
                        int direction, int gather, const void* in, void* out, loong_stream_t stream) {
+  NvtxRange range("loong_headctx_pack");
   if (batch < 0 || cp < 1 || P < 1 || s_local < 0 || heads < 1 || d < 1) return LOONG_ERR_INVALID_ARG;
   if (heads % P || (d * 2) % 16) return LOONG_ERR_INVALID_ARG;
   if (direction != 0 && direction != 1) return LOONG_ERR_INVALID_ARG;

@@ -493,6 +493,7 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
     }
     record_start(stream);
     st = run_exchanged_steps(d, k, v, rk, rv, stream, [&](int t, int buf) {
+      NvtxRange step("fwd ring step %d", t);
       a.t_begin = t;
       a.t_end = t + 1;
       a.kv_held = buf >= 0;
@@ -505,6 +506,7 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   }
   record_start(stream);
   for (int t = 0; t < d.cp; ++t) {
+    NvtxRange step("fwd ring step %d", t);
     a.t_begin = t;
     a.t_end = t + 1;
     kern<<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(mq, mk, mv, a);

@@ -6,6 +6,10 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
+#include <cstdio>
+
 #include "../../include/loong_attn.h"
 #include "ring.cuh"
 
@@ -37,6 +41,20 @@ int make_head_tile_map(CUtensorMap* map, const void* base, int64_t rows, int hea
 // fp32 tensor [rows][heads][d] viewed as (d, heads, rows), box (32, 1, 128),
 // 128-byte swizzle (one box row is 128 bytes).
 int make_f32_tile_map(CUtensorMap* map, const void* base, int64_t rows, int heads, int d);
+
+// An NVTX range (profiler timelines: one per entry point and per ring step)
+// for the lifetime of the object; no cost unless a tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  NvtxRange(const char* fmt, int v) {
+    char buf[48];
+    std::snprintf(buf, sizeof(buf), fmt, v);
+    nvtxRangePushA(buf);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 RingGeom ring_geom(const loong_attn_desc& d);
 // Token/head placement of the descriptor's tensors (natural or rank-major).
