@@ -43,9 +43,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    p.add_argument("--mode", default="fused", choices=["fused", "stepwise", "stepwise-copy"],
+    p.add_argument("--mode", default="fused", choices=["fused", "stepwise", "stepwise-copy", "stepwise-copy-ab"],
                    help="stepwise-copy: one launch per ring step, K/V delivered by device-to-device copies "
-                        "on a side stream (rank-major layout)")
+                        "on a side stream (rank-major layout); -ab: blocks A and B on two streams (two rings)")
     p.add_argument("--layout", default="rank-major", choices=["rank-major", "natural"],
                    help="rank-major: the step repacks in and out around the ring kernels (2D attention)")
     p.add_argument("--no-e2e", action="store_true")
@@ -451,7 +451,8 @@ def run_gpu(args, w, rank, local, world, pg):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    mode = {"fused": ops.MODE_FUSED, "stepwise": ops.MODE_STEPWISE, "stepwise-copy": ops.MODE_STEPWISE_COPY}[args.mode]
+    mode = {"fused": ops.MODE_FUSED, "stepwise": ops.MODE_STEPWISE, "stepwise-copy": ops.MODE_STEPWISE_COPY,
+            "stepwise-copy-ab": ops.MODE_STEPWISE_COPY_AB}[args.mode]
     stream = torch.cuda.current_stream(dev)
     path = TwoDPath(w, mode, args.layout, dev, stream)
     x = inputs.make_inputs(w, device=dev, with_do=True)
@@ -512,7 +513,8 @@ def run_gpu(args, w, rank, local, world, pg):
     ms_total = max_over_ranks(pg, ms_total, dev)
     merge_rec = time_lse_merge(w, path.out["o"], path.lse, stream, dev)
     per_rank = time_per_rank(w, x, stream, dev) if args.per_rank else None
-    exchange = time_exchange_alone(w, path, stream, dev) if mode == ops.MODE_STEPWISE_COPY else None
+    exchange = time_exchange_alone(w, path, stream, dev) if mode in (ops.MODE_STEPWISE_COPY,
+                                                                      ops.MODE_STEPWISE_COPY_AB) else None
     ms_step = ms_total / args.steps
     f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
     b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b) if do_bwd else 0.0

@@ -207,8 +207,7 @@ int loong_attn_check(const loong_attn_desc* d) {
   if (static_cast<int64_t>(d->ring_inner) * d->ring_outer != d->cp) return LOONG_ERR_INVALID_ARG;
   if (d->placement != LOONG_PLACEMENT_ZIGZAG && d->placement != LOONG_PLACEMENT_CONTIGUOUS)
     return LOONG_ERR_INVALID_ARG;
-  if (d->mode != LOONG_MODE_FUSED && d->mode != LOONG_MODE_STEPWISE && d->mode != LOONG_MODE_STEPWISE_COPY)
-    return LOONG_ERR_INVALID_ARG;
+  if (d->mode < LOONG_MODE_STEPWISE || d->mode > LOONG_MODE_STEPWISE_COPY_AB) return LOONG_ERR_INVALID_ARG;
   if (d->layout != LOONG_LAYOUT_NATURAL && d->layout != LOONG_LAYOUT_RANK_MAJOR) return LOONG_ERR_INVALID_ARG;
   const int64_t nblocks = d->placement == LOONG_PLACEMENT_ZIGZAG ? 2 * static_cast<int64_t>(d->cp) : d->cp;
   if (d->seqlen % nblocks) return LOONG_ERR_INVALID_ARG;
@@ -220,7 +219,9 @@ int loong_attn_check(const loong_attn_desc* d) {
   if (!is_pow2_ok_hd(d->head_dim)) return LOONG_ERR_UNSUPPORTED;
   if (d->causal != 0 && d->causal != 1) return LOONG_ERR_INVALID_ARG;
   // the exchange copies whole per-rank chunks: contiguous only in the rank-major layout
-  if (d->mode == LOONG_MODE_STEPWISE_COPY && d->layout != LOONG_LAYOUT_RANK_MAJOR) return LOONG_ERR_UNSUPPORTED;
+  if (is_copy_mode(*d) && d->layout != LOONG_LAYOUT_RANK_MAJOR) return LOONG_ERR_UNSUPPORTED;
+  // two rings need two blocks per rank
+  if (d->mode == LOONG_MODE_STEPWISE_COPY_AB && d->placement != LOONG_PLACEMENT_ZIGZAG) return LOONG_ERR_UNSUPPORTED;
   return LOONG_OK;
 }
 
@@ -231,7 +232,7 @@ size_t loong_attn_workspace_size(const loong_attn_desc* d, int pass) {
   const size_t rows = static_cast<size_t>(d->batch) * d->hq * d->seqlen;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   // STEPWISE_COPY: two receive buffers each for K and V, bf16
-  const size_t recv = d->mode == LOONG_MODE_STEPWISE_COPY ? 4 * up(kv_elems * 2) : 0;
+  const size_t recv = is_copy_mode(*d) ? 4 * up(kv_elems * 2) : 0;
   if (pass == 0) return d->mode == LOONG_MODE_FUSED ? 0 : up(q_elems * 4) + recv;
   if (pass != 1) return 0;
   const size_t stats = 2 * static_cast<size_t>(d->batch) * d->hq * stat_row_len(ring_geom(*d));
@@ -265,7 +266,7 @@ int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const
   cudaError_t e = cudaMemsetAsync(o_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   if ((st = launch_fill_f32(lse, d->batch * d->hq * d->seqlen, -INFINITY, stream)) != LOONG_OK) return st;
-  void* recv = d->mode == LOONG_MODE_STEPWISE_COPY ? static_cast<uint8_t*>(ws) + ((q_elems * 4 + 255) & ~255LL)
+  void* recv = is_copy_mode(*d) ? static_cast<uint8_t*>(ws) + ((q_elems * 4 + 255) & ~255LL)
                                                    : nullptr;
   if ((st = launch_fwd(*d, q, k, v, o, lse, o_acc, stream, 0, -1, recv)) != LOONG_OK) return st;
   return launch_f32_to_bf16(o_acc, o, q_elems, stream);
@@ -308,7 +309,7 @@ int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const
   float* dvec = reinterpret_cast<float*>(w + up(q_elems * 4));
   float* dk_acc = reinterpret_cast<float*>(w + up(q_elems * 4) + up(stats * 4));
   float* dv_acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dk_acc) + up(kv_elems * 4));
-  void* recv = d->mode == LOONG_MODE_STEPWISE_COPY ? reinterpret_cast<uint8_t*>(dv_acc) + up(kv_elems * 4) : nullptr;
+  void* recv = is_copy_mode(*d) ? reinterpret_cast<uint8_t*>(dv_acc) + up(kv_elems * 4) : nullptr;
   return launch_bwd(*d, q, k, v, o, lse, dout, dq, dk, dv, dq_acc, dvec, dk_acc, dv_acc, stream, recv);
 }
 

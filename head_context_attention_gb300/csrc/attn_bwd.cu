@@ -671,7 +671,7 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
     record_stop(stream);
     return check_launch();
   }
-  if (d.mode == LOONG_MODE_STEPWISE_COPY) {
+  if (is_copy_mode(d)) {
     // receive buffers K0, K1, V0, V1, each the size of K (exchange.h); dK, dV
     // are accumulated at the owner's rows, so only K and V travel
     const size_t kv_bytes = static_cast<size_t>(rows) * vkv * D * 2;

@@ -480,7 +480,7 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
     record_stop(stream);
     return check_launch();
   }
-  if (d.mode == LOONG_MODE_STEPWISE_COPY) {
+  if (is_copy_mode(d)) {
     // receive buffers K0, K1, V0, V1, each the size of K
     const size_t kv_bytes = static_cast<size_t>(rows) * lay.view_heads(d.hkv) * D * 2;
     uint8_t* rb = static_cast<uint8_t*>(kv_recv);

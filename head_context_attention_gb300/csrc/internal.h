@@ -57,6 +57,10 @@ struct NvtxRange {
 };
 
 RingGeom ring_geom(const loong_attn_desc& d);
+// STEPWISE_COPY or STEPWISE_COPY_AB: the K/V exchange goes through receive buffers.
+inline bool is_copy_mode(const loong_attn_desc& d) {
+  return d.mode == LOONG_MODE_STEPWISE_COPY || d.mode == LOONG_MODE_STEPWISE_COPY_AB;
+}
 // Token/head placement of the descriptor's tensors (natural or rank-major).
 Layout layout_of(const loong_attn_desc& d);
 

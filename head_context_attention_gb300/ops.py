@@ -25,7 +25,7 @@ LOONG_ERR_CUDA = -4
 LOONG_ERR_DEVICE_TIMEOUT = -5
 LOONG_ERR_DEVICE_CHECK = -6
 PLACEMENT_CONTIGUOUS, PLACEMENT_ZIGZAG = 0, 1
-MODE_STEPWISE, MODE_FUSED, MODE_STEPWISE_COPY = 0, 1, 2
+MODE_STEPWISE, MODE_FUSED, MODE_STEPWISE_COPY, MODE_STEPWISE_COPY_AB = 0, 1, 2, 3
 LAYOUT_NATURAL, LAYOUT_RANK_MAJOR = 0, 1
 
 EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loong_attn_check",

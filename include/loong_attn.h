@@ -68,7 +68,7 @@ typedef enum {
 } loong_status;
 
 enum { LOONG_PLACEMENT_CONTIGUOUS = 0, LOONG_PLACEMENT_ZIGZAG = 1 };
-enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1, LOONG_MODE_STEPWISE_COPY = 2 };
+enum { LOONG_MODE_STEPWISE = 0, LOONG_MODE_FUSED = 1, LOONG_MODE_STEPWISE_COPY = 2, LOONG_MODE_STEPWISE_COPY_AB = 3 };
 enum { LOONG_LAYOUT_NATURAL = 0, LOONG_LAYOUT_RANK_MAJOR = 1 };
 
 /*
@@ -107,6 +107,10 @@ enum { LOONG_LAYOUT_NATURAL = 0, LOONG_LAYOUT_RANK_MAJOR = 1 };
  *                     owner's rows (their return trip is not copied).  The
  *                     side stream and its events are one per device: calls in
  *                     this mode on one device must not overlap.
+ *                     STEPWISE_COPY_AB (ZIGZAG placement): the same with the
+ *                     guide's two rings ([G] section 3): the block A and block
+ *                     B halves of every chunk travel on two independent side
+ *                     streams.  Results equal STEPWISE's.
  *   softmax_scale     <= 0 selects 1/sqrt(head_dim) ([G] "Step 3",
  *                     forward_local_attention).
  *   layout            LOONG_LAYOUT_NATURAL or LOONG_LAYOUT_RANK_MAJOR (the

@@ -61,7 +61,8 @@ def _desc(**kw):
     ("causal", 0, ops.LOONG_OK),
     ("causal", 2, ops.LOONG_ERR_INVALID_ARG),
     ("placement", 7, ops.LOONG_ERR_INVALID_ARG),
-    ("mode", 3, ops.LOONG_ERR_INVALID_ARG),
+    ("mode", 5, ops.LOONG_ERR_INVALID_ARG),
+    ("mode", ops.MODE_STEPWISE_COPY_AB, ops.LOONG_ERR_UNSUPPORTED),   # needs the rank-major layout
     ("batch", 0, ops.LOONG_ERR_INVALID_ARG),
     ("layout", 2, ops.LOONG_ERR_INVALID_ARG),
     ("mode", ops.MODE_STEPWISE_COPY, ops.LOONG_ERR_UNSUPPORTED),   # needs the rank-major layout
@@ -148,3 +149,15 @@ def test_selftest_wait_limit_validated_before_any_cuda_call(loong_lib):
     L = ops.lib()
     for bad in (0, 1000001):
         assert L.loong_selftest_wait_timeout(bad, None) == ops.LOONG_ERR_INVALID_ARG
+
+
+def test_two_ring_copy_mode_needs_paired_blocks(loong_lib):
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    d = ops.make_desc(w, ops.MODE_STEPWISE_COPY_AB, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_check(d) == ops.LOONG_OK
+    one = ops.make_desc(w, ops.MODE_STEPWISE_COPY, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_workspace_size(d, 1) == ops.loong_attn_workspace_size(one, 1)
+    d.placement = ops.PLACEMENT_CONTIGUOUS
+    assert ops.loong_attn_check(d) == ops.LOONG_ERR_UNSUPPORTED
+    d = ops.make_desc(w, 4, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_check(d) == ops.LOONG_ERR_INVALID_ARG

@@ -122,19 +122,24 @@ def test_fwd_ranks_union_is_the_full_forward(cuda_device, name, layout):
 @pytest.mark.parametrize("name", ["d128-double-ring", "contiguous", "ragged-blocks", "batch2", "g8-cp8",
                                   "tiny-blocks", "single-rank"])
 def test_stepwise_copy_equals_stepwise(cuda_device, name):
-    """STEPWISE_COPY reads every step's K/V from the receive buffers the
-    exchange copies filled; the arithmetic is STEPWISE's, so the results are
-    equal (dQ up to its reduction order)."""
+    """STEPWISE_COPY (one ring) and STEPWISE_COPY_AB (blocks A and B on two
+    rings) read every step's K/V from the receive buffers the exchange copies
+    filled; the arithmetic is STEPWISE's, so the results are equal (dQ up to
+    its reduction order)."""
     w = _workload(name)
     x = inputs.make_inputs(w, device="cuda", with_do=True)
     p = {n: _pack(w, x[n]) for n in ("q", "k", "v", "do")}
     rm = ops.LAYOUT_RANK_MAJOR
     res = {}
-    for mode in (ops.MODE_STEPWISE, ops.MODE_STEPWISE_COPY):
+    # the two-ring variant needs two blocks per rank (paired placement)
+    modes = [ops.MODE_STEPWISE, ops.MODE_STEPWISE_COPY] + ([ops.MODE_STEPWISE_COPY_AB] if w.placement == 1 else [])
+    for mode in modes:
         o, lse = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=rm)
         res[mode] = (o, lse) + ops.attn_bwd(w, p["q"], p["k"], p["v"], o, lse, p["do"], mode=mode, layout=rm)
     assert ops.loong_get_device_status() == ops.LOONG_OK
-    a, b = res[ops.MODE_STEPWISE], res[ops.MODE_STEPWISE_COPY]
-    for i in (0, 1, 3, 4):   # O, LSE, dK, dV
-        assert torch.equal(a[i], b[i]), i
-    assert _within_one_bf16_spacing(b[2], a[2])
+    a = res[ops.MODE_STEPWISE]
+    for mode in modes[1:]:
+        b = res[mode]
+        for i in (0, 1, 3, 4):   # O, LSE, dK, dV
+            assert torch.equal(a[i], b[i]), (mode, i)
+        assert _within_one_bf16_spacing(b[2], a[2])
