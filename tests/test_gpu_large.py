@@ -106,3 +106,33 @@ def test_full_size_sampled_parity(cuda_device, name):
     err = np.abs(dv_sum - do_grp)
     bound = noise(dv) + 1e-3 * np.abs(do_grp)
     assert np.all(err <= bound), (err.max(), float((err / bound).max()))
+
+
+def _within_one_bf16_spacing(a, b):
+    """One bf16 spacing plus 2^-16 max|b| (fp32 dQ sums reordered between runs)."""
+    a, b = a.double(), b.double()
+    bound = 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 2.0 ** -16 * b.abs().max()
+    return bool(((a - b).abs() <= bound).all())
+
+
+def test_full_size_bench_pass_equals_natural(cuda_device):
+    """The pass bench.py times at full size (repack into the rank-major layout,
+    FUSED ring forward + backward on it, repack out) gives the natural-layout
+    results that test_full_size_sampled_parity checks against the oracle: O,
+    LSE, dK, dV bit for bit, dQ up to its fp32 reduction order."""
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    x = inputs.make_inputs(w, device="cuda", with_do=True)
+    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"])
+    p = {n: ops.headctx_pack(x[n], w.cp, w.hp, 1) for n in ("q", "k", "v", "do")}
+    del x
+    rm = ops.LAYOUT_RANK_MAJOR
+    o2, lse2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], layout=rm)
+    dq2, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], layout=rm)
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    un = lambda t: ops.headctx_unpack(t, w.batch, w.cp, w.hp, 1)
+    assert torch.equal(lse2, lse)
+    assert torch.equal(un(o2), o)
+    assert torch.equal(un(dk2), dk)
+    assert torch.equal(un(dv2), dv)
+    assert _within_one_bf16_spacing(un(dq2), dq)
