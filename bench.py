@@ -78,11 +78,17 @@ KERNEL_SOURCES = ("attn_fwd.cu", "attn_bwd.cu", "ptx.cuh", "ring.cuh")
 
 
 def kernel_source_hash():
+    """SHA-256 of the kernel sources' code: `//` comments, trailing blanks and
+    empty lines are dropped, so a comment-only edit keeps the recorded counters."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "head_context_attention_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "head_context_attention_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = re.sub(r"//.*$", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 

@@ -1,7 +1,7 @@
 // attn_bwd.cu -- backward ring-step attention on tcgen05 tensor cores.
 //
-// The gradient of causal softmax attention (plain chain rule; the pages give no
-// backward).  One CTA owns one 128-key tile of one kv head and walks every
+// The gradient of softmax attention, causal or not (plain chain rule; the pages
+// give no backward).  One CTA owns one 128-key tile of one kv head and walks every
 // (query tile, query head of the group) that attends to it, in the order the
 // key/value chunk travels around the ring: step t visits ring rank
 // dst(j, t), the rank that holds source j's K/V at step t.  Per iteration:
@@ -17,7 +17,10 @@
 // left in the accumulators (STEPWISE, one launch per step; a step maps ranks to
 // sources one to one, so no two CTAs share a tile).  The compute warps form P^T
 // as soon as S^T is ready, while dP^T is still on the tensor cores, and drain
-// dQ while dK is computed.
+// dQ while dK is computed.  Tensors are addressed through a Layout (natural or
+// rank-major, ring.cuh); in STEPWISE_COPY modes the K/V tile is read from the
+// plane of the rank that holds it at the launch's step (exchange.h), while dK
+// and dV go to the owner's rows.
 //
 // Warp roles (352 threads): warps 0-3 and 4-7 form two groups that each cover
 // all 128 TMEM lanes; group w handles query columns [64w, 64w+64) of S^T/dP^T

@@ -13,7 +13,11 @@
 // and l to the new maximum, which is the log-sum-exp merge written in
 // unnormalised form.  In STEPWISE mode the launch covers one ring step and the
 // epilogue merges the step's normalised result into an fp32 accumulator by
-// log-sum-exp.
+// log-sum-exp.  Non-causal descriptors walk every key tile and mask only the
+// ragged tail of a block.  Q, K, V and O are addressed through a Layout
+// (natural or rank-major, ring.cuh); in STEPWISE_COPY modes K and V are read
+// from the query rank's plane of the receive buffers the exchange filled
+// (exchange.h).  A launch may cover the query rows of a range of ring ranks.
 //
 // Warp roles (320 threads): warps 0-3 softmax for head slot 0, warps 4-7 for
 // head slot 1 (warp w reads TMEM lanes 32*(w%4)..+31, the rows it owns),

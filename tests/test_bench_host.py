@@ -99,3 +99,16 @@ def test_rank_pairs_match_the_oracle_schedule(placement, seqlen, cp):
     w = inputs.WORKLOADS["tiny-gqa-s1k"].with_(seqlen=seqlen, cp=cp, ring_inner=cp, ring_outer=1)
     for c in range(cp):
         assert bench.rank_pairs(w, placement, c) == schedule.pair_work(seqlen, cp, c, placement)
+
+
+def test_kernel_source_hash_ignores_comments(tmp_path, monkeypatch):
+    src = tmp_path / "head_context_attention_gb300" / "csrc"
+    src.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES:
+        (src / f).write_text("int a = 1;  // one\n\nint b = 2;\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    (src / bench.KERNEL_SOURCES[0]).write_text("// a new comment\nint a = 1;  // changed\n   \nint b = 2;\n")
+    assert bench.kernel_source_hash() == h0
+    (src / bench.KERNEL_SOURCES[0]).write_text("int a = 3;\nint b = 2;\n")
+    assert bench.kernel_source_hash() != h0
