@@ -357,7 +357,9 @@ def cpu_sample(w, seconds, arrays):
         flops += float(np.sum(3.5 * 4.0 * (rows + 1) * w.head_dim))
         rows_done += chunk
     el = time.perf_counter() - t0
-    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+    rate = flops / el
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "extrapolated_full_step_s": round(w.flops / rate, 1),
             "sample": f"{rows_done} query rows of head 0 at S={w.seqlen} (forward row + dQ row, float64), "
                       f"{el:.1f} s"}
 
