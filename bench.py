@@ -564,7 +564,8 @@ def run_gpu(args, w, rank, local, world, pg):
                    "step": ("repack Q,K,V,dO -> ring fwd + bwd on the rank-major layout -> repack O,dQ,dK,dV"
                             if path.rank_major else "ring fwd + bwd on the natural layout"),
                    "parallelism": f"replicas x{world} (each rank: all hp x cp ranks emulated)",
-                   "l2": "inputs exceed L2 (Q and dO 1 GiB each at this size); no flush",
+                   "l2": f"inputs exceed L2 (Q {w.batch * w.seqlen * w.hq * w.head_dim * 2 / 2**20:.0f} MiB vs 126 MiB "
+                         "of L2); no flush",
                    "flops_per_step": flops_step},
         "pct_of_peak": round(100.0 * tflops / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": f"ring_{dominant}_kernel", "achieved": round(dom_tf, 2),
@@ -664,7 +665,7 @@ def main(argv=None):
     w = inputs.WORKLOADS[args.workload]
     if args.seqlen:
         w = w.with_(seqlen=args.seqlen, name=f"{w.name}@S={args.seqlen}")
-    w = w.with_(backward=not args.fwd_only)
+    w = w.with_(backward=w.backward and not args.fwd_only)   # a forward-only workload stays forward only
     if args.non_causal:
         w = w.with_(causal=False, name=f"{w.name}@non-causal")
     rank = int(os.environ.get("RANK", "0"))
