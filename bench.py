@@ -571,7 +571,9 @@ def run_gpu(args, w, rank, local, world, pg):
         "roofline": {"bound": "tensor", "kernel": f"ring_{dominant}_kernel", "achieved": round(dom_tf, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(dom_tf / peak, 4),
                      "peak_kind": f"bf16 sustained, of {peaks['source']}",
-                     "traffic": recorded_traffic(f"ring_{dominant}_kernel", w.name, args.layout),
+                     # the record holds FUSED launches (one launch per pass)
+                     "traffic": (recorded_traffic(f"ring_{dominant}_kernel", w.name, args.layout)
+                                 if mode == ops.MODE_FUSED and w.causal else None),
                      "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"},
         "kernels": kernels,
         "clocks": clocks,
