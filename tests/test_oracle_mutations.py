@@ -4,7 +4,7 @@ least one pin test then fails."""
 import numpy as np
 import pytest
 
-from oracle import attention, merge, repack, ring, schedule
+from oracle import attention, merge, repack, schedule
 from tests import test_oracle_attention as TA
 from tests import test_oracle_merge as TM
 from tests import test_oracle_repack as TR
