@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--layout", default="rank-major", choices=["rank-major", "natural"],
                    help="rank-major: the step repacks in and out around the ring kernels (2D attention)")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-overlap", action=argparse.BooleanOptionalAction, default=True,
+                   help="end-to-end leg: host copies on copy streams under the compute (default) or in series")
     p.add_argument("--per-rank", action=argparse.BooleanOptionalAction, default=True,
                    help="after the timed steps, time each emulated ring rank's forward on its own")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -408,10 +410,14 @@ class TwoDPath:
             n += (4 if self.do_bwd else 3) + (4 if self.do_bwd else 1)
         return n
 
-    def pack_in(self, x):
+    FWD_IN, BWD_IN, FWD_OUT, BWD_OUT = ("q", "k", "v"), ("do",), ("o",), ("dq", "dk", "dv")
+
+    def pack_in(self, x, names=None):
+        """Repack the named inputs (default: every input of the pass) into the per-rank layout."""
         if not self.rank_major:
             return
-        names = ("q", "k", "v", "do") if self.do_bwd else ("q", "k", "v")
+        if names is None:
+            names = self.FWD_IN + (self.BWD_IN if self.do_bwd else ())
         for n in names:
             self._pack(x[n], self.kt[n], n, 0)
 
@@ -434,10 +440,12 @@ class TwoDPath:
         self.ops.loong_attn_bwd(self.desc, t["q"], t["k"], t["v"], o, self.lse, t["do"], g["dq"], g["dk"],
                                 g["dv"], self.ws1, self.stream)
 
-    def unpack_out(self):
+    def unpack_out(self, names=None):
+        """Repack the named outputs (default: every output of the pass) back to the natural layout."""
         if not self.rank_major:
             return
-        names = ("o", "dq", "dk", "dv") if self.do_bwd else ("o",)
+        if names is None:
+            names = self.FWD_OUT + (self.BWD_OUT if self.do_bwd else ())
         for n in names:
             self._pack(self.kt[n], self.out[n], n, 1)
 
@@ -483,6 +491,8 @@ def run_gpu(args, w, rank, local, world, pg):
     # The end-to-end leg runs before the clock-sampled region: host copies made
     # after an nvidia-smi sampling loop has run measured 6-8x slower.
     e2e = None if args.no_e2e else run_e2e(args, w, path, dev, stream, world, pg, x, e2e_bufs)
+    if e2e is not None:
+        e2e["check"] = e2e_outputs_match(path, e2e_bufs[1], step, dev)
 
     # Timed region: K steps; per-kernel events for the forward and backward kernels.
     mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -599,9 +609,10 @@ def pinned_buffers(w, path, x):
     """Pinned host copies of the inputs and pinned host buffers for the outputs."""
     import torch
 
-    host_in = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in x.items()}
-    for n, t in x.items():
-        host_in[n].copy_(t)
+    names = path.FWD_IN + (path.BWD_IN if w.backward else ())
+    host_in = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
+    for n in names:
+        host_in[n].copy_(x[n])
     outs = dict(path.out, lse=path.lse)
     if not w.backward:
         outs = {"o": path.out["o"], "lse": path.lse}
@@ -609,53 +620,120 @@ def pinned_buffers(w, path, x):
     return host_in, host_out, outs
 
 
+def e2e_outputs_match(path, host_out, step, dev):
+    """The last end-to-end step's results, read back to the host, against a
+    device-only pass over the same inputs: O, LSE, dK, dV bit for bit (their
+    kernels are deterministic), dQ (summed by unordered reductions) within
+    2^-7 of its largest magnitude.  A copy that raced its kernels fails."""
+    import torch
+
+    step()
+    torch.cuda.synchronize(dev)
+    ok = True
+    for n, h in host_out.items():
+        d = (path.lse if n == "lse" else path.out[n]).cpu()
+        if n == "dq":
+            ok &= bool((h.float() - d.float()).abs().max() <= 2.0 ** -7 * d.float().abs().max())
+        else:
+            ok &= torch.equal(h, d)
+    return ok
+
+
 def run_e2e(args, w, path, dev, stream, world, pg, x, bufs):
     """Same metric through the public API with host buffers: every step copies
     Q, K, V, dO (natural layout) from pinned host memory and O, LSE, dQ, dK, dV
-    (natural layout) back, around the same pass as the timed step."""
+    (natural layout) back, around the same kernels as the timed step.
+
+    Overlapped (default): the copies run on two copy streams.  Step i+1's
+    inputs arrive (into the other of two device input sets) and step i's
+    results leave while the GPU computes; within a step dO arrives during the
+    forward and O, LSE leave during the backward.  Every copy of every step,
+    the first step's inputs and the last step's results included, lies inside
+    the timed region.  ``--no-e2e-overlap`` issues the same copies and kernels
+    on one stream, in series."""
     import torch
 
     host_in, host_out, outs = bufs
-    dev_in = {n: torch.empty_like(t) for n, t in x.items()}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    overlap = args.e2e_overlap
+    dev_in = [{n: torch.empty_like(x[n]) for n in host_in} for _ in range(2 if overlap else 1)]
+    s_in = torch.cuda.Stream(dev) if overlap else stream
+    s_out = torch.cuda.Stream(dev) if overlap else stream
+    fwd_in = [n for n in host_in if n in path.FWD_IN]
+    bwd_in = [n for n in host_in if n not in path.FWD_IN]
+    fwd_out = [n for n in host_out if n in path.FWD_OUT + ("lse",)]
+    bwd_out = [n for n in host_out if n not in path.FWD_OUT + ("lse",)]
+    names = ("in0", "in_f", "in1", "c0", "f", "c1", "out0", "fo", "out0b", "out1", "used")
 
-    phases = ("h2d", "repack_in", "fwd", "bwd", "repack_out", "d2h")
+    def run(nsteps):
+        ev = [{k: torch.cuda.Event(enable_timing=True) for k in names} for _ in range(nsteps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
 
-    def step(ev=None):
-        mark = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
-        mark(0)
-        for n in dev_in:
-            dev_in[n].copy_(host_in[n], non_blocking=True)
-        mark(1)
-        path.pack_in(dev_in)
-        mark(2)
-        path.fwd(dev_in)
-        mark(3)
-        path.bwd(dev_in)
-        mark(4)
-        path.unpack_out()
-        mark(5)
-        for n in host_out:
-            host_out[n].copy_(outs[n], non_blocking=True)
-        mark(6)
+        def copies(s, pairs, done):
+            with torch.cuda.stream(s):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+                done.record(s)
 
-    for _ in range(max(1, args.warmup)):
-        step()
+        def issue_h2d(i):
+            buf, e = dev_in[i % len(dev_in)], ev[i]
+            s_in.wait_event(start if i < len(dev_in) else ev[i - len(dev_in)]["used"])
+            e["in0"].record(s_in)
+            copies(s_in, [(buf[n], host_in[n]) for n in fwd_in], e["in_f"])
+            copies(s_in, [(buf[n], host_in[n]) for n in bwd_in], e["in1"])
+
+        issue_h2d(0)
+        for i in range(nsteps):
+            buf, e, prev = dev_in[i % len(dev_in)], ev[i], ev[i - 1] if i > 0 else None
+            stream.wait_event(e["in_f"])
+            e["c0"].record(stream)
+            if overlap and i + 1 < nsteps:
+                issue_h2d(i + 1)
+            if prev:
+                stream.wait_event(prev["fo"])      # the forward rewrites LSE (and O, natural layout)
+            path.pack_in(buf, path.FWD_IN)
+            path.fwd(buf)
+            path.unpack_out(path.FWD_OUT)
+            e["f"].record(stream)
+            s_out.wait_event(e["f"])
+            e["out0"].record(s_out)
+            copies(s_out, [(host_out[n], outs[n]) for n in fwd_out], e["fo"])
+            stream.wait_event(e["in1"])
+            if path.do_bwd:
+                if prev and not path.rank_major:
+                    stream.wait_event(prev["out1"])    # the natural-layout backward writes dQ, dK, dV itself
+                path.pack_in(buf, path.BWD_IN)
+                path.bwd(buf)
+            e["used"].record(stream)
+            if prev:
+                stream.wait_event(prev["out1"])
+            if path.do_bwd:
+                path.unpack_out(path.BWD_OUT)
+            e["c1"].record(stream)
+            s_out.wait_event(e["c1"])
+            e["out0b"].record(s_out)
+            copies(s_out, [(host_out[n], outs[n]) for n in bwd_out], e["out1"])
+            if not overlap and i + 1 < nsteps:
+                issue_h2d(i + 1)
+        stream.wait_event(ev[nsteps - 1]["out1"])
+        stop.record(stream)
+        return start, stop, ev
+
+    run(max(1, args.warmup))
     torch.cuda.synchronize(dev)
     barrier(pg)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    b.record(stream)
+    start, stop, ev = run(args.steps)
     torch.cuda.synchronize(dev)
-    ms = max_over_ranks(pg, a.elapsed_time(b), dev) / args.steps
-    phase_ms = {p: round(statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs), 3) for j, p in enumerate(phases)}
+    ms = max_over_ranks(pg, start.elapsed_time(stop), dev) / args.steps
+    span = lambda *pairs: round(statistics.mean(sum(e[a].elapsed_time(e[b]) for a, b in pairs) for e in ev), 3)
     return {"value": round(w.flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "phase_ms": phase_ms}
+            "copies": ("two copy streams overlapped with compute, inputs double-buffered" if overlap
+                       else "in series with compute on one stream"),
+            "phase_ms": {"h2d": span(("in0", "in1")), "compute": span(("c0", "c1")),
+                         "d2h": span(("out0", "fo"), ("out0b", "out1"))}}
 
 
 def main(argv=None):

@@ -68,6 +68,28 @@ int device_ready() {
   return LOONG_OK;
 }
 
+// Device memory of the current device (cudaMalloc'd or managed).  Host memory,
+// pinned or not, is refused: a kernel could read pinned memory over the
+// chip-to-chip link, but far slower, and an unregistered pointer not at all.
+bool on_device(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // not sticky; keep it from a later launch check
+    return false;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
+
+template <typename... T>
+bool all_on_device(const T*... p) {
+  return (on_device(p) && ...);
+}
+
 }  // namespace
 
 int cuda_fail(cudaError_t e) {
@@ -259,6 +281,7 @@ int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const
   const size_t need = loong_attn_workspace_size(d, 0);
   if (need && (!ws || ws_bytes < need || !aligned16(ws))) return LOONG_ERR_WORKSPACE;
   if ((st = device_ready()) != LOONG_OK) return st;
+  if (!all_on_device(q, k, v, o, lse) || (need && !on_device(ws))) return LOONG_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (d->mode == LOONG_MODE_FUSED) return launch_fwd(*d, q, k, v, o, lse, nullptr, stream);
   const int64_t q_elems = d->batch * d->seqlen * d->hq * d->head_dim;
@@ -283,6 +306,7 @@ int loong_attn_fwd_ranks(const loong_attn_desc* d, int32_t rank_begin, int32_t r
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return LOONG_ERR_INVALID_ARG;
   if ((st = device_ready()) != LOONG_OK) return st;
+  if (!all_on_device(q, k, v, o, lse)) return LOONG_ERR_INVALID_ARG;
   return launch_fwd(*d, q, k, v, o, lse, nullptr, reinterpret_cast<cudaStream_t>(stream_), rank_begin, rank_end);
 }
 
@@ -299,6 +323,9 @@ int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const
   const size_t need = loong_attn_workspace_size(d, 1);
   if (!ws || ws_bytes < need || !aligned16(ws)) return LOONG_ERR_WORKSPACE;
   if ((st = device_ready()) != LOONG_OK) return st;
+  for (const void* p : ptrs)
+    if (!on_device(p)) return LOONG_ERR_INVALID_ARG;
+  if (!on_device(ws)) return LOONG_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t q_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hq * d->head_dim;
@@ -325,6 +352,7 @@ int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts, const float* o_par
     return LOONG_ERR_INVALID_ARG;
   int st = device_ready();
   if (st != LOONG_OK) return st;
+  if (!all_on_device(o_parts, lse_parts, lse_out) || !on_device(o_out)) return LOONG_ERR_INVALID_ARG;
   return launch_lse_merge(rows, d, n_parts, o_parts, lse_parts, o_out, lse_out, out_bf16,
                           reinterpret_cast<cudaStream_t>(stream));
 }
@@ -342,6 +370,7 @@ int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s_local, in
   if (!in || !out || !aligned16(in) || !aligned16(out)) return LOONG_ERR_INVALID_ARG;
   int st = device_ready();
   if (st != LOONG_OK) return st;
+  if (!on_device(in) || !on_device(out)) return LOONG_ERR_INVALID_ARG;
   return launch_headctx_pack(batch, cp, P, s_local, heads, d, direction, gather, in, out,
                              reinterpret_cast<cudaStream_t>(stream));
 }

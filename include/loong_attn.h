@@ -12,7 +12,10 @@
  *
  * Conventions shared by every entry point
  *   - Pointers named q, k, v, o, dout, dq, dk, dv, lse, ws, in, out, o_parts,
- *     lse_parts, o_out, lse_out are DEVICE pointers owned by the caller.  The
+ *     lse_parts, o_out, lse_out are DEVICE pointers owned by the caller:
+ *     memory of the current device, from cudaMalloc or managed.  A host
+ *     pointer (pinned or not) or another device's memory is refused with
+ *     LOONG_ERR_INVALID_ARG before any work is enqueued.  The
  *     library allocates no device memory, keeps no state between calls except a
  *     cached device query, a loaded tensor-map encoder, one device error word
  *     and (STEPWISE_COPY) one side stream with its events per device, and
@@ -52,7 +55,8 @@ typedef struct CUstream_st* loong_stream_t;
 
 typedef enum {
   LOONG_OK = 0,
-  LOONG_ERR_INVALID_ARG = -1,     /* null pointer, bad size or divisibility   */
+  LOONG_ERR_INVALID_ARG = -1,     /* null, misaligned or non-device pointer,
+                                     bad size or divisibility                 */
   LOONG_ERR_WORKSPACE = -2,       /* ws_bytes smaller than the workspace size */
   LOONG_ERR_UNSUPPORTED = -3,     /* valid but not built: head_dim, a mode /
                                      layout pairing, device is not compute
