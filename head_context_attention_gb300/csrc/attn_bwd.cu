@@ -50,7 +50,7 @@ struct BwdCfg {
   static constexpr int ATOM_BYTES = kTile * 128;  // 16 KB
   static constexpr int TILE_BYTES = kTile * D * 2;
   static constexpr int DS_BYTES = kTile * kTile * 2;  // dS^T tile, bf16 [keys][queries]
-  static constexpr int NBARS = 1 + 2 * NS + 14;
+  static constexpr int NBARS = 1 + 4 * NS + 13;
   static constexpr int STAT_BYTES = 2 * kTile * 4;  // LSE*log2e and D of one query tile
   // Tiles first (1024-byte aligned, checked at run time), then the row
   // statistics stages, the barriers, the TMEM base address and the abort flag.
@@ -63,6 +63,12 @@ struct BwdCfg {
   static constexpr int DQ_BOXES = D / 32;
   static constexpr int BOX_BYTES = kTile * 128;
   static constexpr int BOXES_PER_STAGE = TILE_BYTES / BOX_BYTES;
+  // Group 1's dQ columns land in the dO half of the stage, which dV(i) has
+  // finished reading before dQ(i) exists.  At d = 64 group 1 stages them at
+  // once and the reducer adds that half first (measured faster); at d = 128
+  // both groups stage after dK(i) and the reducer takes the whole tile at once
+  // (measured faster there).
+  static constexpr bool EARLY_O = D == 64;
 };
 
 // dK and dV build up in tensor memory; every kFlush iterations they are added
@@ -119,11 +125,14 @@ __global__ void __launch_bounds__(352, 1)
   uint64_t* dq_full = ds_full + 1;      // dQ(i) in R1           (MMA -> warps)
   uint64_t* dq_empty = dq_full + 1;     // R1 drained            (warps -> MMA)
   uint64_t* dk_done = dq_empty + 1;     // dK(i) done: Q/dO stage free for staging
-  uint64_t* staged = dk_done + 1;       // dQ(i) staged in smem  (warps -> reducer)
-  uint64_t* acc_full = staged + 1;      // dK/dV ready to flush  (MMA -> warps)
+  uint64_t* acc_full = dk_done + 1;     // dK/dV ready to flush  (MMA -> warps)
   uint64_t* acc_empty = acc_full + 1;   // dK/dV flushed         (warps -> MMA)
   uint64_t* done_bar = acc_empty + 1;
   uint64_t* drain = done_bar + 1;
+  // per stage, so that neither runs a phase ahead of the reducer: a stage is
+  // staged into again only after the reducer has read it and it was reloaded
+  uint64_t* staged_q = drain + 1;       // NS: dQ(i) staged (EARLY_O: group 0's Q half)  (warps -> reducer)
+  uint64_t* staged_o = staged_q + C::NS;  // NS: EARLY_O: group 1's dO half             (warps -> reducer)
   uint32_t& tmem_base_sh = *reinterpret_cast<uint32_t*>(bars + C::NBARS);
   int& abort_sh = *(reinterpret_cast<int*>(bars + C::NBARS) + 1);
   volatile int* abort_flag = &abort_sh;
@@ -163,7 +172,10 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(dq_full, 1);
     mbar_init(dq_empty, 8);
     mbar_init(dk_done, 1);
-    mbar_init(staged, 8);
+    for (int st = 0; st < C::NS; ++st) {
+      mbar_init(&staged_q[st], C::EARLY_O ? 4 : 8);
+      mbar_init(&staged_o[st], 4);
+    }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
     mbar_init(done_bar, 1);
@@ -332,9 +344,18 @@ __global__ void __launch_bounds__(352, 1)
         const bool red_ok =
             in_bounds(qrow64 >= 0 && qrow64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
         const int qrow = static_cast<int>(qrow64);
-        if (!mbar_wait(staged, i & 1, abort_flag, a.err)) break;
+        if constexpr (C::EARLY_O) {
+          // the dO half first: it is staged without waiting for dK(i)
+          if (!mbar_wait(&staged_o[s], (i / C::NS) & 1, abort_flag, a.err)) break;
 #pragma unroll
-        for (int box = 0; box < C::DQ_BOXES; ++box) {
+          for (int box = C::BOXES_PER_STAGE; box < C::DQ_BOXES; ++box)
+            if (red_ok)
+              tma_reduce_add_3d(&tmDQ, sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES,
+                                box * 32, hc, qrow);
+        }
+        if (!mbar_wait(&staged_q[s], (i / C::NS) & 1, abort_flag, a.err)) break;
+#pragma unroll
+        for (int box = 0; box < (C::EARLY_O ? C::BOXES_PER_STAGE : C::DQ_BOXES); ++box) {
           const uint8_t* base = box < C::BOXES_PER_STAGE
                                     ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
                                     : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
@@ -510,7 +531,9 @@ __global__ void __launch_bounds__(352, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dq_empty);
-        if (!warp_wait(dk_done, i & 1)) {
+        // group 0 stages into the Q half, which dK(i) may still read; group 1
+        // into the dO half, whose last reader dV(i) retired before dQ(i)
+        if ((grp == 0 || !C::EARLY_O) && !warp_wait(dk_done, i & 1)) {
           ok = false;
           break;
         }
@@ -533,7 +556,7 @@ __global__ void __launch_bounds__(352, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(staged);
+        if (lane == 0) mbar_arrive(grp == 0 || !C::EARLY_O ? &staged_q[s] : &staged_o[s]);
       }
 
       // ---- every kFlush iterations: fold dV / dK into the fp32 accumulators
