@@ -50,7 +50,7 @@ def parse_args(argv=None):
                    help="rank-major: the step repacks in and out around the ring kernels (2D attention)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--e2e-overlap", action=argparse.BooleanOptionalAction, default=True,
-                   help="end-to-end leg: host copies on copy streams under the compute (default) or in series")
+                   help="end-to-end leg: copies overlapped with the kernels (default) or each call synchronised")
     p.add_argument("--per-rank", action=argparse.BooleanOptionalAction, default=True,
                    help="after the timed steps, time each emulated ring rank's forward on its own")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -617,7 +617,7 @@ def pinned_buffers(w, path, x):
     if not w.backward:
         outs = {"o": path.out["o"], "lse": path.lse}
     host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
-    return host_in, host_out, outs
+    return host_in, host_out
 
 
 def e2e_outputs_match(path, host_out, step, dev):
@@ -640,100 +640,75 @@ def e2e_outputs_match(path, host_out, step, dev):
 
 
 def run_e2e(args, w, path, dev, stream, world, pg, x, bufs):
-    """Same metric through the public API with host buffers: every step copies
-    Q, K, V, dO (natural layout) from pinned host memory and O, LSE, dQ, dK, dV
-    (natural layout) back, around the same kernels as the timed step.
-
-    Overlapped (default): the copies run on two copy streams.  Step i+1's
-    inputs arrive (into the other of two device input sets) and step i's
-    results leave while the GPU computes; within a step dO arrives during the
-    forward and O, LSE leave during the backward.  Every copy of every step,
-    the first step's inputs and the last step's results included, lies inside
-    the timed region.  ``--no-e2e-overlap`` issues the same copies and kernels
-    on one stream, in series."""
+    """Same metric through the C ABI with host buffers: each step is one
+    loong_attn_2d_host call, natural-layout Q, K, V, dO in pinned host memory
+    to O, LSE, dQ, dK, dV in pinned host memory.  The library's two copy
+    streams carry the copies; consecutive calls alternate the two device input
+    slots, so a step's inputs arrive and the previous step's results leave
+    while the kernels run.  Every copy of every step lies inside the timed
+    region, which ends when the last step's results are in host memory.
+    ``--no-e2e-overlap`` synchronises after every call instead (copies and
+    kernels in series)."""
     import torch
 
-    host_in, host_out, outs = bufs
+    from head_context_attention_gb300 import ops
+
+    host_in, host_out = bufs
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     overlap = args.e2e_overlap
-    dev_in = [{n: torch.empty_like(x[n]) for n in host_in} for _ in range(2 if overlap else 1)]
-    s_in = torch.cuda.Stream(dev) if overlap else stream
-    s_out = torch.cuda.Stream(dev) if overlap else stream
-    fwd_in = [n for n in host_in if n in path.FWD_IN]
-    bwd_in = [n for n in host_in if n not in path.FWD_IN]
-    fwd_out = [n for n in host_out if n in path.FWD_OUT + ("lse",)]
-    bwd_out = [n for n in host_out if n not in path.FWD_OUT + ("lse",)]
-    names = ("in0", "in_f", "in1", "c0", "f", "c1", "out0", "fo", "out0b", "out1", "used")
+    desc = path.desc
+    ws = torch.empty(ops.loong_attn_2d_host_workspace_size(desc, 1 if w.backward else 0), dtype=torch.uint8,
+                     device=dev)
+    grads = (host_out["dq"], host_out["dk"], host_out["dv"]) if w.backward else (None, None, None)
+
+    def call(slot, done):
+        ops.loong_attn_2d_host(desc, slot, host_in["q"], host_in["k"], host_in["v"], host_in.get("do"),
+                               host_out["o"], host_out["lse"], *grads, ws, stream, done)
 
     def run(nsteps):
-        ev = [{k: torch.cuda.Event(enable_timing=True) for k in names} for _ in range(nsteps)]
+        dones = [torch.cuda.Event() for _ in range(nsteps)]
+        for e in dones:
+            e.record(stream)   # torch creates the event on its first record; the library records it again
+        torch.cuda.synchronize(dev)
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record(stream)
-
-        def copies(s, pairs, done):
-            with torch.cuda.stream(s):
-                for dst, src in pairs:
-                    dst.copy_(src, non_blocking=True)
-                done.record(s)
-
-        def issue_h2d(i):
-            buf, e = dev_in[i % len(dev_in)], ev[i]
-            s_in.wait_event(start if i < len(dev_in) else ev[i - len(dev_in)]["used"])
-            e["in0"].record(s_in)
-            copies(s_in, [(buf[n], host_in[n]) for n in fwd_in], e["in_f"])
-            copies(s_in, [(buf[n], host_in[n]) for n in bwd_in], e["in1"])
-
-        issue_h2d(0)
         for i in range(nsteps):
-            buf, e, prev = dev_in[i % len(dev_in)], ev[i], ev[i - 1] if i > 0 else None
-            stream.wait_event(e["in_f"])
-            e["c0"].record(stream)
-            if overlap and i + 1 < nsteps:
-                issue_h2d(i + 1)
-            if prev:
-                stream.wait_event(prev["fo"])      # the forward rewrites LSE (and O, natural layout)
-            path.pack_in(buf, path.FWD_IN)
-            path.fwd(buf)
-            path.unpack_out(path.FWD_OUT)
-            e["f"].record(stream)
-            s_out.wait_event(e["f"])
-            e["out0"].record(s_out)
-            copies(s_out, [(host_out[n], outs[n]) for n in fwd_out], e["fo"])
-            stream.wait_event(e["in1"])
-            if path.do_bwd:
-                if prev and not path.rank_major:
-                    stream.wait_event(prev["out1"])    # the natural-layout backward writes dQ, dK, dV itself
-                path.pack_in(buf, path.BWD_IN)
-                path.bwd(buf)
-            e["used"].record(stream)
-            if prev:
-                stream.wait_event(prev["out1"])
-            if path.do_bwd:
-                path.unpack_out(path.BWD_OUT)
-            e["c1"].record(stream)
-            s_out.wait_event(e["c1"])
-            e["out0b"].record(s_out)
-            copies(s_out, [(host_out[n], outs[n]) for n in bwd_out], e["out1"])
-            if not overlap and i + 1 < nsteps:
-                issue_h2d(i + 1)
-        stream.wait_event(ev[nsteps - 1]["out1"])
+            call(i % 2, dones[i] if overlap else None)
+            if not overlap:
+                stream.synchronize()
+        if overlap:
+            stream.wait_event(dones[-1])
         stop.record(stream)
-        return start, stop, ev
+        torch.cuda.synchronize(dev)
+        return start.elapsed_time(stop)
+
+    # the copy speed of the moment: one plain H2D of the inputs and one D2H of the outputs
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    dev_in = {n: torch.empty_like(t, device=dev) for n, t in host_in.items()}
+    dev_out = {n: torch.empty_like(t, device=dev) for n, t in host_out.items()}
+    a.record(stream)
+    for n in dev_in:
+        dev_in[n].copy_(host_in[n], non_blocking=True)
+    b.record(stream)
+    for n in dev_out:
+        host_out[n].copy_(dev_out[n], non_blocking=True)
+    c.record(stream)
+    torch.cuda.synchronize(dev)
+    copy_ms = {"h2d": round(a.elapsed_time(b), 3), "d2h": round(b.elapsed_time(c), 3)}
+    del dev_in, dev_out
 
     run(max(1, args.warmup))
-    torch.cuda.synchronize(dev)
     barrier(pg)
-    start, stop, ev = run(args.steps)
-    torch.cuda.synchronize(dev)
-    ms = max_over_ranks(pg, start.elapsed_time(stop), dev) / args.steps
-    span = lambda *pairs: round(statistics.mean(sum(e[a].elapsed_time(e[b]) for a, b in pairs) for e in ev), 3)
+    ms = max_over_ranks(pg, run(args.steps), dev) / args.steps
+    if ops.loong_get_device_status(stream) != ops.LOONG_OK:
+        raise SystemExit("device status after the end-to-end leg")
     return {"value": round(w.flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "copies": ("two copy streams overlapped with compute, inputs double-buffered" if overlap
-                       else "in series with compute on one stream"),
-            "phase_ms": {"h2d": span(("in0", "in1")), "compute": span(("c0", "c1")),
-                         "d2h": span(("out0", "fo"), ("out0b", "out1"))}}
+            "api": "loong_attn_2d_host (C ABI, pinned host buffers)",
+            "copies": ("library copy streams overlapped with the kernels, two input slots" if overlap
+                       else "in series: each call synchronised before the next"),
+            "copy_alone_ms": copy_ms}
 
 
 def main(argv=None):

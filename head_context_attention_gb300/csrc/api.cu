@@ -60,6 +60,8 @@ bool is_pow2_ok_hd(int d) { return d == 64 || d == 128; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 // Every CUDA-touching entry point checks the device first.
 int device_ready() {
   DeviceCache* c = device_cache();
@@ -85,12 +87,20 @@ bool on_device(const void* p) {
   return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
 }
 
+// Host memory: pinned (registered) or pageable.
+bool in_host_memory(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
 template <typename... T>
 bool all_on_device(const T*... p) {
   return (on_device(p) && ...);
 }
-
-}  // namespace
 
 int cuda_fail(cudaError_t e) {
   std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", cudaGetErrorName(e),

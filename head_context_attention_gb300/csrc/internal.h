@@ -24,6 +24,15 @@ int check_launch();
 void record_start(cudaStream_t s);
 void record_stop(cudaStream_t s);
 
+// LOONG_OK when the current device is usable (compute capability 10.3), else
+// LOONG_ERR_UNSUPPORTED or LOONG_ERR_CUDA; every CUDA-touching entry point
+// checks it first.
+int device_ready();
+// Memory of the current device (cudaMalloc'd or managed).
+bool on_device(const void* p);
+// Host memory, pinned or pageable.
+bool in_host_memory(const void* p);
+
 // Device address of the library's error word on the current device.
 unsigned* device_error_word();
 

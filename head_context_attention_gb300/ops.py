@@ -32,6 +32,7 @@ EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loo
            "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_fwd_ranks",
            "loong_attn_bwd",
            "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack",
+           "loong_attn_2d_host_workspace_size", "loong_attn_2d_host",
            "loong_set_timing_events", "loong_get_device_status", "loong_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 32 << 20   # LOONG_NOALLOC_SCRATCH_BYTES
 
@@ -82,6 +83,9 @@ def lib():
         L.loong_lse_merge.argtypes = [I64, I32, I32, P, P, P, P, ctypes.c_int, P]
         L.loong_headctx_pack.argtypes = [I64, I32, I32, I64, I32, I32, ctypes.c_int, ctypes.c_int,
                                          P, P, P]
+        L.loong_attn_2d_host_workspace_size.restype = SZ
+        L.loong_attn_2d_host_workspace_size.argtypes = [D, ctypes.c_int]
+        L.loong_attn_2d_host.argtypes = [D, I32, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
         L.loong_set_timing_events.argtypes = [P, P]
         L.loong_get_device_status.argtypes = [P]
         L.loong_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
@@ -158,6 +162,21 @@ def loong_lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
 def loong_headctx_pack(x, out, batch, cp, P, s_local, heads, d, direction, gather, stream=None):
     return _check("loong_headctx_pack", lib().loong_headctx_pack(
         batch, cp, P, s_local, heads, d, direction, gather, _ptr(x), _ptr(out), _stream(stream)))
+
+
+def loong_attn_2d_host_workspace_size(desc, pass_):
+    return lib().loong_attn_2d_host_workspace_size(ctypes.byref(desc), pass_)
+
+
+def loong_attn_2d_host(desc, slot, q, k, v, dout, o, lse, dq, dk, dv, ws, stream=None, done_event=None):
+    """One 2D-attention pass from host tensors to host tensors (pinned for
+    overlap); dout=None runs the forward alone.  done_event: a recorded
+    torch.cuda.Event marking the host outputs ready, or None."""
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+    ev = None if done_event is None else ctypes.c_void_p(done_event.cuda_event)
+    return _check("loong_attn_2d_host", lib().loong_attn_2d_host(
+        ctypes.byref(desc), slot, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse), _ptr(dq),
+        _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream(stream), ev))
 
 
 def loong_set_timing_events(start=None, stop=None):

@@ -284,6 +284,56 @@ LOONG_API int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s
                        loong_stream_t stream);
 
 /*
+ * Device workspace, in bytes, of loong_attn_2d_host for `desc`: pass 0 runs
+ * the forward alone, pass 1 the forward and the backward; 0 for an invalid
+ * descriptor.  Host-only.  It holds two sets of natural-layout inputs (the
+ * slots), the natural-layout outputs and LSE, the rank-major tensors of the
+ * pass (RANK_MAJOR) and the workspaces of loong_attn_fwd / loong_attn_bwd,
+ * each part on a 256-byte boundary.
+ */
+LOONG_API size_t loong_attn_2d_host_workspace_size(const loong_attn_desc* desc, int pass);
+
+/*
+ * One whole 2D-attention pass from host memory to host memory: the inputs
+ * travel to the device, the Ulysses repack moves them into every emulated
+ * rank's layout ([G] "The Scalability Limits of DeepSpeed Ulysses"), the ring
+ * forward (and backward) run on it, and the outputs are repacked and travel
+ * back.  With a NATURAL descriptor the ring kernels read and write the
+ * natural layout and there is no repack.
+ *   q, k, v, dout   host inputs, natural layout [B,S,H,d] bf16.  dout == NULL
+ *                   runs the forward alone (dq, dk, dv must then be NULL).
+ *   o, lse          host outputs: bf16 [B,S,Hq,d] and fp32 [B,Hq,S].
+ *   dq, dk, dv      host outputs, bf16, the layouts of q and k.
+ *   slot            0 or 1: which of the workspace's two device input sets
+ *                   this call fills.  Alternate it between consecutive calls
+ *                   so that a call's inputs can arrive while the previous
+ *                   call's kernels still read theirs.
+ *   ws, ws_bytes    device workspace of loong_attn_2d_host_workspace_size
+ *                   bytes (pass 1 when dout != NULL, else pass 0).
+ *   done_event      a cudaEvent_t of the caller, or NULL.  Non-NULL: it is
+ *                   recorded once every output has reached host memory, and
+ *                   `stream` does not wait for the output copies, so the next
+ *                   call's kernels overlap them.  NULL: `stream` waits for the
+ *                   output copies before its later work.
+ * Every copy runs on one of two library-owned copy streams (host to device,
+ * device to host), ordered against the kernels on `stream` by events: a
+ * call's input copies start when the call is made, once the slot's previous
+ * inputs have been read; dO arrives while the forward runs, and O and LSE
+ * leave while the backward runs.  Pinned host memory (cudaHostAlloc /
+ * cudaHostRegister) lets the copies overlap the kernels; pageable memory is
+ * accepted but copies synchronously.  The caller must not change the inputs
+ * or read the outputs before the call's work has finished (done_event, or
+ * `stream` when done_event is NULL).  Calls on one device are serialised by
+ * the library (one enqueue at a time).  Device pointers in the host
+ * arguments, a slot other than 0 or 1 and null pointers give
+ * LOONG_ERR_INVALID_ARG; a short workspace gives LOONG_ERR_WORKSPACE.
+ */
+LOONG_API int loong_attn_2d_host(const loong_attn_desc* desc, int32_t slot, const void* q, const void* k,
+                                 const void* v, const void* dout, void* o, float* lse, void* dq, void* dk,
+                                 void* dv, void* ws, size_t ws_bytes, loong_stream_t stream,
+                                 void* done_event);
+
+/*
  * Measurement aid.  When both are non-NULL, the calling thread's next
  * loong_attn_fwd / loong_attn_bwd calls record `start_event` on their stream
  * just before launching the main ring-attention kernel(s) and `stop_event`

@@ -161,3 +161,43 @@ def test_two_ring_copy_mode_needs_paired_blocks(loong_lib):
     assert ops.loong_attn_check(d) == ops.LOONG_ERR_UNSUPPORTED
     d = ops.make_desc(w, 4, layout=ops.LAYOUT_RANK_MAJOR)
     assert ops.loong_attn_check(d) == ops.LOONG_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("layout", [ops.LAYOUT_NATURAL, ops.LAYOUT_RANK_MAJOR])
+def test_2d_host_workspace_sizes(loong_lib, layout):
+    """Two slots of natural inputs, the natural outputs and LSE, the rank-major
+    tensors (RANK_MAJOR only) and the ring workspaces, each 256-byte aligned."""
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    d = ops.make_desc(w, ops.MODE_FUSED, layout=layout)
+    up = lambda x: (x + 255) // 256 * 256
+    qb = w.seqlen * w.hq * w.head_dim * 2
+    kvb = w.seqlen * w.hkv * w.head_dim * 2
+    lse = w.hq * w.seqlen * 4
+    rm = layout == ops.LAYOUT_RANK_MAJOR
+    fwd = 2 * (up(qb) + 2 * up(kvb)) + up(qb) + up(lse) + (up(qb) + 2 * up(kvb) + up(qb) if rm else 0)
+    both = 2 * (2 * up(qb) + 2 * up(kvb)) + 2 * up(qb) + 2 * up(kvb) + up(lse) + \
+        ((3 * up(qb) + 2 * up(kvb)) + (up(qb) + 2 * up(kvb)) if rm else 0) + ops.loong_attn_workspace_size(d, 1)
+    assert ops.loong_attn_2d_host_workspace_size(d, 0) == fwd + ops.loong_attn_workspace_size(d, 0)
+    assert ops.loong_attn_2d_host_workspace_size(d, 1) == both
+    assert ops.loong_attn_2d_host_workspace_size(d, 2) == 0
+    assert ops.loong_attn_2d_host_workspace_size(_desc(hq=30), 1) == 0
+
+
+def test_2d_host_validation_before_any_cuda_call(loong_lib):
+    d = ops.make_desc(inputs.WORKLOADS["tiny-gqa-s1k"], layout=ops.LAYOUT_RANK_MAJOR)
+    L = ops.lib()
+    need = ops.loong_attn_2d_host_workspace_size(d, 1)
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    ws = ctypes.c_void_p(1 << 20)   # never dereferenced: every case below fails before any CUDA call
+    call = lambda slot, dout, grads, ws_, n: L.loong_attn_2d_host(
+        ctypes.byref(d), slot, p, p, p, dout, p, p, *(grads or (None, None, None)), ws_, n, None, None)
+    assert call(2, p, (p, p, p), ws, need) == ops.LOONG_ERR_INVALID_ARG        # slot
+    assert call(-1, p, (p, p, p), ws, need) == ops.LOONG_ERR_INVALID_ARG
+    assert call(0, p, (p, None, p), ws, need) == ops.LOONG_ERR_INVALID_ARG     # a gradient missing
+    assert call(0, None, (p, p, p), ws, need) == ops.LOONG_ERR_INVALID_ARG     # gradients without dO
+    assert call(0, p, (p, p, p), ws, need - 256) == ops.LOONG_ERR_WORKSPACE
+    assert call(0, p, (p, p, p), None, need) == ops.LOONG_ERR_WORKSPACE
+    assert call(0, p, (p, p, p), ctypes.c_void_p((1 << 20) + 16), need) == ops.LOONG_ERR_WORKSPACE  # alignment
+    assert L.loong_attn_2d_host(ctypes.byref(d), 0, None, p, p, p, p, p, p, p, p, ws, need, None, None) == \
+        ops.LOONG_ERR_INVALID_ARG
