@@ -407,7 +407,7 @@ class TwoDPath:
         fused = self.desc.mode == ops.MODE_FUSED
         n = (1 if fused else w.cp + 2) + (((3 if fused else w.cp + 4)) if self.do_bwd else 0)
         if self.rank_major:
-            n += (4 if self.do_bwd else 3) + (4 if self.do_bwd else 1)
+            n += 2   # one repack launch in, one out
         return n
 
     FWD_IN, BWD_IN, FWD_OUT, BWD_OUT = ("q", "k", "v"), ("do",), ("o",), ("dq", "dk", "dv")
@@ -418,13 +418,13 @@ class TwoDPath:
             return
         if names is None:
             names = self.FWD_IN + (self.BWD_IN if self.do_bwd else ())
-        for n in names:
-            self._pack(x[n], self.kt[n], n, 0)
+        self._pack([x[n] for n in names], [self.kt[n] for n in names], names, 0)
 
-    def _pack(self, src, dst, n, direction):
+    def _pack(self, srcs, dsts, names, direction):
+        """One launch repacks every named tensor (the pass's one all-to-all per direction)."""
         w = self.w
-        self.ops.loong_headctx_pack(src, dst, w.batch, w.cp, w.hp, self.s_local, self.heads[n], w.head_dim,
-                                    direction, self.gather, self.stream)
+        self.ops.loong_headctx_pack_n(srcs, dsts, w.batch, w.cp, w.hp, self.s_local, [self.heads[n] for n in names],
+                                      w.head_dim, direction, self.gather, self.stream)
 
     def fwd(self, x):
         t = self.kt if self.rank_major else x
@@ -446,8 +446,7 @@ class TwoDPath:
             return
         if names is None:
             names = self.FWD_OUT + (self.BWD_OUT if self.do_bwd else ())
-        for n in names:
-            self._pack(self.kt[n], self.out[n], n, 1)
+        self._pack([self.kt[n] for n in names], [self.out[n] for n in names], names, 1)
 
     def repack_bytes(self):
         """Algorithmic bytes of the repacks of one step (read + write), in and out."""

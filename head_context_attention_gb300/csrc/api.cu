@@ -367,22 +367,33 @@ int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts, const float* o_par
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
-int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s_local, int32_t heads, int32_t d,
-                       int direction, int gather, const void* in, void* out, loong_stream_t stream) {
+int loong_headctx_pack_n(int32_t n, int64_t batch, int32_t cp, int32_t P, int64_t s_local, const int32_t* heads,
+                         int32_t d, int direction, int gather, const void* const* in, void* const* out,
+                         loong_stream_t stream) {
   NvtxRange range("loong_headctx_pack");
-  if (batch < 0 || cp < 1 || P < 1 || s_local < 0 || heads < 1 || d < 1) return LOONG_ERR_INVALID_ARG;
-  if (heads % P || (d * 2) % 16) return LOONG_ERR_INVALID_ARG;
+  if (n < 1 || n > 4 || !heads || !in || !out) return LOONG_ERR_INVALID_ARG;
+  if (batch < 0 || cp < 1 || P < 1 || s_local < 0 || d < 1) return LOONG_ERR_INVALID_ARG;
+  for (int t = 0; t < n; ++t)
+    if (heads[t] < 1 || heads[t] % P) return LOONG_ERR_INVALID_ARG;
+  if ((d * 2) % 16) return LOONG_ERR_INVALID_ARG;
   if (direction != 0 && direction != 1) return LOONG_ERR_INVALID_ARG;
   if (gather < 0 || gather > 2) return LOONG_ERR_INVALID_ARG;
   const int64_t S = static_cast<int64_t>(cp) * P * s_local;
   if (gather == 1 && (S % (2 * cp))) return LOONG_ERR_INVALID_ARG;
   if (batch == 0 || s_local == 0) return LOONG_OK;
-  if (!in || !out || !aligned16(in) || !aligned16(out)) return LOONG_ERR_INVALID_ARG;
+  for (int t = 0; t < n; ++t)
+    if (!in[t] || !out[t] || !aligned16(in[t]) || !aligned16(out[t])) return LOONG_ERR_INVALID_ARG;
   int st = device_ready();
   if (st != LOONG_OK) return st;
-  if (!on_device(in) || !on_device(out)) return LOONG_ERR_INVALID_ARG;
-  return launch_headctx_pack(batch, cp, P, s_local, heads, d, direction, gather, in, out,
+  for (int t = 0; t < n; ++t)
+    if (!on_device(in[t]) || !on_device(out[t])) return LOONG_ERR_INVALID_ARG;
+  return launch_headctx_pack(n, batch, cp, P, s_local, heads, d, direction, gather, in, out,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s_local, int32_t heads, int32_t d,
+                       int direction, int gather, const void* in, void* out, loong_stream_t stream) {
+  return loong_headctx_pack_n(1, batch, cp, P, s_local, &heads, d, direction, gather, &in, &out, stream);
 }
 
 int loong_set_timing_events(void* start_event, void* stop_event) {

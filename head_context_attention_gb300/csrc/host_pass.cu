@@ -147,7 +147,7 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
   const bool rm = d->layout == LOONG_LAYOUT_RANK_MAJOR;
   const int64_t s_local = d->seqlen / (static_cast<int64_t>(d->cp) * d->hp);
   const int gather = d->placement == LOONG_PLACEMENT_ZIGZAG ? 1 : 2;
-  const int heads[8] = {d->hq, d->hkv, d->hkv, d->hq, d->hq, d->hq, d->hkv, d->hkv};  // q k v dO o dq dk dv
+  const int32_t heads[8] = {d->hq, d->hkv, d->hkv, d->hq, d->hq, d->hq, d->hkv, d->hkv};  // q k v dO o dq dk dv
   cudaError_t e;
 #define LOONG_TRY(x)                           \
   do {                                         \
@@ -159,12 +159,17 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
   auto d2h = [&](void* dst, size_t src, size_t bytes) {
     return cudaMemcpyAsync(dst, at(src), bytes, cudaMemcpyDeviceToHost, hp->d2h);
   };
-  // natural <-> rank-major repack of tensor t (0..7) between natural buffer `nat` and its rank-major copy
-  auto repack = [&](int t, size_t nat, int direction) {
-    const void* src = direction == 0 ? at(nat) : at(L.kt[t]);
-    void* dst = direction == 0 ? at(L.kt[t]) : at(nat);
-    return loong_headctx_pack(d->batch, d->cp, d->hp, s_local, heads[t], d->head_dim, direction, gather, src, dst,
-                              stream_);
+  // natural <-> rank-major repack, in one launch, of the tensors t0 .. t0+n-1 (0..7) between their natural
+  // buffers nat[] and their rank-major copies
+  auto repack = [&](int t0, int n, const size_t* nat, int direction) {
+    const void* src[4];
+    void* dst[4];
+    for (int i = 0; i < n; ++i) {
+      src[i] = direction == 0 ? at(nat[i]) : at(L.kt[t0 + i]);
+      dst[i] = direction == 0 ? at(L.kt[t0 + i]) : at(nat[i]);
+    }
+    return loong_headctx_pack_n(n, d->batch, d->cp, d->hp, s_local, heads + t0, d->head_dim, direction, gather,
+                                src, dst, stream_);
   };
   const size_t* in = L.in[slot];
 
@@ -182,9 +187,7 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
   // ---- forward; it rewrites LSE (and O in the natural layout), which the
   // previous call's output copies must have read
   LOONG_TRY(cudaStreamWaitEvent(stream, hp->fwd_in, 0));
-  if (rm)
-    for (int t = 0; t < 3; ++t)
-      if ((st = repack(t, in[t], 0)) != LOONG_OK) return st;
+  if (rm && (st = repack(0, 3, in, 0)) != LOONG_OK) return st;
   if (pass == 0 && rm) LOONG_TRY(cudaEventRecord(hp->slot_free[slot], stream));
   LOONG_TRY(cudaStreamWaitEvent(stream, hp->o_lse_out, 0));
   float* lse_dev = static_cast<float*>(at(L.lse_off));
@@ -193,7 +196,7 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
     if ((st = loong_attn_fwd(d, at(L.kt[0]), at(L.kt[1]), at(L.kt[2]), at(L.kt[4]), lse_dev, ws_fwd, L.ws_fwd_bytes,
                              stream_)) != LOONG_OK)
       return st;
-    if ((st = repack(4, L.out[0], 1)) != LOONG_OK) return st;
+    if ((st = repack(4, 1, L.out, 1)) != LOONG_OK) return st;
   } else if ((st = loong_attn_fwd(d, at(in[0]), at(in[1]), at(in[2]), at(L.out[0]), lse_dev, ws_fwd,
                                   L.ws_fwd_bytes, stream_)) != LOONG_OK) {
     return st;
@@ -211,14 +214,13 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
     LOONG_TRY(cudaStreamWaitEvent(stream, hp->bwd_in, 0));
     void* ws_bwd = at(L.ws_bwd);
     if (rm) {
-      if ((st = repack(3, in[3], 0)) != LOONG_OK) return st;
+      if ((st = repack(3, 1, in + 3, 0)) != LOONG_OK) return st;
       LOONG_TRY(cudaEventRecord(hp->slot_free[slot], stream));
       if ((st = loong_attn_bwd(d, at(L.kt[0]), at(L.kt[1]), at(L.kt[2]), at(L.kt[4]), lse_dev, at(L.kt[3]),
                                at(L.kt[5]), at(L.kt[6]), at(L.kt[7]), ws_bwd, L.ws_bwd_bytes, stream_)) != LOONG_OK)
         return st;
       LOONG_TRY(cudaStreamWaitEvent(stream, hp->grads_out, 0));
-      for (int t = 5; t < 8; ++t)
-        if ((st = repack(t, L.out[t - 4], 1)) != LOONG_OK) return st;
+      if ((st = repack(5, 3, L.out + 1, 1)) != LOONG_OK) return st;
     } else {
       LOONG_TRY(cudaStreamWaitEvent(stream, hp->grads_out, 0));
       if ((st = loong_attn_bwd(d, at(in[0]), at(in[1]), at(in[2]), at(L.out[0]), lse_dev, at(in[3]),

@@ -91,9 +91,9 @@ int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t strea
 int launch_lse_merge(int64_t rows, int d, int n_parts, const float* o_parts,
                      const float* lse_parts, void* o_out, float* lse_out, int out_bf16,
                      cudaStream_t stream);
-int launch_headctx_pack(int64_t batch, int cp, int P, int64_t s_local, int heads, int d,
-                        int direction, int gather, const void* in, void* out,
-                        cudaStream_t stream);
+// n (1..4) tensors of the same mesh and direction, heads[t] heads each, one launch.
+int launch_headctx_pack(int n, int64_t batch, int cp, int P, int64_t s_local, const int* heads, int d,
+                        int direction, int gather, const void* const* in, void* const* out, cudaStream_t stream);
 // Backward row statistics: for every (batch, query head, token) the values
 // LSE*log2(e) and D = rowsum(dO*O), in [B*Hq][stat_row_len] arrays (LSE part
 // first, then D) where block b's tokens start at b*stat_block_pad(blk), so a

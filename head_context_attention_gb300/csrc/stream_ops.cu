@@ -288,16 +288,33 @@ __device__ __forceinline__ int64_t pack_row_source(const PackGeom& g, int64_t ro
 constexpr int kPackThreads = 256;
 constexpr int kPackMaxRows = 256;
 
+// Up to four tensors repacked by one launch: the same mesh and direction,
+// their own head counts.  Their tiles are numbered one after the other
+// (tile_begin) and the grid strides over all of them.
+constexpr int kPackMaxTensors = 4;
+struct PackSet {
+  PackGeom g[kPackMaxTensors];
+  const uint4* in[kPackMaxTensors];
+  uint4* out[kPackMaxTensors];
+  int64_t total_rows[kPackMaxTensors];
+  int64_t tile_begin[kPackMaxTensors + 1];
+  int n;
+};
+
 template <int DIR>
-__global__ void __launch_bounds__(kPackThreads) pack_kernel(PackGeom g, int64_t total_rows, const uint4* __restrict__ in,
-                                                           uint4* __restrict__ out) {
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constant__ PackSet set) {
   __shared__ int64_t src_row[kPackMaxRows];
   constexpr int U = 8;
-  const int64_t ntiles = (total_rows + g.tile_rows - 1) / g.tile_rows;
-  const int64_t plane = g.s_grp * g.Hp * g.vpr;  // vectors per (n, p) plane of the packed layout
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t row0 = tile * g.tile_rows;
-    const int rows = static_cast<int>(min(static_cast<int64_t>(g.tile_rows), total_rows - row0));
+  for (int64_t tile = blockIdx.x; tile < set.tile_begin[set.n]; tile += gridDim.x) {
+    int t = 0;
+#pragma unroll
+    for (int i = 1; i < kPackMaxTensors; ++i) t += (i < set.n && tile >= set.tile_begin[i]) ? 1 : 0;
+    const PackGeom& g = set.g[t];
+    const uint4* __restrict__ in = set.in[t];
+    uint4* __restrict__ out = set.out[t];
+    const int64_t plane = g.s_grp * g.Hp * g.vpr;  // vectors per (n, p) plane of the packed layout
+    const int64_t row0 = (tile - set.tile_begin[t]) * g.tile_rows;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(g.tile_rows), set.total_rows[t] - row0));
     __syncthreads();  // the previous tile's offsets are no longer read
     for (int r = threadIdx.x; r < rows; r += kPackThreads) src_row[r] = pack_row_source<DIR>(g, row0 + r);
     __syncthreads();
@@ -438,40 +455,49 @@ int launch_lse_merge(int64_t rows, int d, int n_parts, const float* o_parts, con
   return check_launch();
 }
 
-int launch_headctx_pack(int64_t batch, int cp, int P, int64_t s_local, int heads, int d, int direction,
-                        int gather, const void* in, void* out, cudaStream_t stream) {
-  PackGeom g;
-  g.batch = batch;
-  g.s_local = s_local;
-  g.s_grp = static_cast<int64_t>(P) * s_local;
-  g.seqlen = static_cast<int64_t>(cp) * g.s_grp;
-  g.blk = gather == 1 ? g.seqlen / (2 * cp) : g.seqlen / cp;
-  g.cp = cp;
-  g.P = P;
-  g.H = heads;
-  g.Hp = heads / P;
-  g.vpr = d * 2 / 16;
-  g.gather = gather;
-  const int64_t total_rows = direction == 0 ? batch * cp * P * g.s_grp : batch * g.seqlen;
-  if (total_rows == 0) return LOONG_OK;
-  const int64_t w = direction == 0 ? static_cast<int64_t>(g.Hp) * g.vpr : static_cast<int64_t>(heads) * g.vpr;
-  // a tile of about 2048 vectors (32 KB); the in-tile vector index stays in 32 bits
-  if (w > (1 << 20)) return LOONG_ERR_UNSUPPORTED;
-  g.W = static_cast<int>(w);
-  g.tile_rows = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kPackMaxRows, 2048 / w)));
-  g.fW = make_fastdiv(static_cast<uint32_t>(g.W));
-  g.fRv = make_fastdiv(static_cast<uint32_t>(g.Hp * g.vpr));
-  g.in_vecs = g.out_vecs = batch * g.seqlen * heads * g.vpr;  // both directions move the whole tensor
-  g.err = device_error_word();
-  if (!g.err) return LOONG_ERR_CUDA;
-  const int64_t ntiles = (total_rows + g.tile_rows - 1) / g.tile_rows;
+int launch_headctx_pack(int n, int64_t batch, int cp, int P, int64_t s_local, const int* heads, int d,
+                        int direction, int gather, const void* const* in, void* const* out, cudaStream_t stream) {
+  if (n < 1 || n > kPackMaxTensors) return LOONG_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return LOONG_ERR_CUDA;
+  PackSet set{};
+  set.n = n;
+  set.tile_begin[0] = 0;
+  for (int t = 0; t < n; ++t) {
+    PackGeom& g = set.g[t];
+    g.batch = batch;
+    g.s_local = s_local;
+    g.s_grp = static_cast<int64_t>(P) * s_local;
+    g.seqlen = static_cast<int64_t>(cp) * g.s_grp;
+    g.blk = gather == 1 ? g.seqlen / (2 * cp) : g.seqlen / cp;
+    g.cp = cp;
+    g.P = P;
+    g.H = heads[t];
+    g.Hp = heads[t] / P;
+    g.vpr = d * 2 / 16;
+    g.gather = gather;
+    const int64_t total_rows = direction == 0 ? batch * cp * P * g.s_grp : batch * g.seqlen;
+    const int64_t w = direction == 0 ? static_cast<int64_t>(g.Hp) * g.vpr : static_cast<int64_t>(g.H) * g.vpr;
+    // a tile of about 2048 vectors (32 KB); the in-tile vector index stays in 32 bits
+    if (w > (1 << 20)) return LOONG_ERR_UNSUPPORTED;
+    g.W = static_cast<int>(w);
+    g.tile_rows = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kPackMaxRows, 2048 / w)));
+    g.fW = make_fastdiv(static_cast<uint32_t>(g.W));
+    g.fRv = make_fastdiv(static_cast<uint32_t>(g.Hp * g.vpr));
+    g.in_vecs = g.out_vecs = batch * g.seqlen * g.H * g.vpr;  // both directions move the whole tensor
+    g.err = err;
+    set.in[t] = static_cast<const uint4*>(in[t]);
+    set.out[t] = static_cast<uint4*>(out[t]);
+    set.total_rows[t] = total_rows;
+    set.tile_begin[t + 1] = set.tile_begin[t] + (total_rows + g.tile_rows - 1) / g.tile_rows;
+  }
+  const int64_t ntiles = set.tile_begin[n];
+  if (ntiles == 0) return LOONG_OK;
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(num_sms()) * 8));
   if (direction == 0)
-    pack_kernel<0><<<grid, kPackThreads, 0, stream>>>(g, total_rows, static_cast<const uint4*>(in),
-                                                      static_cast<uint4*>(out));
+    pack_kernel<0><<<grid, kPackThreads, 0, stream>>>(set);
   else
-    pack_kernel<1><<<grid, kPackThreads, 0, stream>>>(g, total_rows, static_cast<const uint4*>(in),
-                                                      static_cast<uint4*>(out));
+    pack_kernel<1><<<grid, kPackThreads, 0, stream>>>(set);
   return check_launch();
 }
 

@@ -31,7 +31,7 @@ LAYOUT_NATURAL, LAYOUT_RANK_MAJOR = 0, 1
 EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loong_attn_check",
            "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_fwd_ranks",
            "loong_attn_bwd",
-           "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack",
+           "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack", "loong_headctx_pack_n",
            "loong_attn_2d_host_workspace_size", "loong_attn_2d_host",
            "loong_set_timing_events", "loong_get_device_status", "loong_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 32 << 20   # LOONG_NOALLOC_SCRATCH_BYTES
@@ -83,6 +83,8 @@ def lib():
         L.loong_lse_merge.argtypes = [I64, I32, I32, P, P, P, P, ctypes.c_int, P]
         L.loong_headctx_pack.argtypes = [I64, I32, I32, I64, I32, I32, ctypes.c_int, ctypes.c_int,
                                          P, P, P]
+        L.loong_headctx_pack_n.argtypes = [I32, I64, I32, I32, I64, ctypes.POINTER(ctypes.c_int32), I32,
+                                           ctypes.c_int, ctypes.c_int, ctypes.POINTER(P), ctypes.POINTER(P), P]
         L.loong_attn_2d_host_workspace_size.restype = SZ
         L.loong_attn_2d_host_workspace_size.argtypes = [D, ctypes.c_int]
         L.loong_attn_2d_host.argtypes = [D, I32, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
@@ -162,6 +164,16 @@ def loong_lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
 def loong_headctx_pack(x, out, batch, cp, P, s_local, heads, d, direction, gather, stream=None):
     return _check("loong_headctx_pack", lib().loong_headctx_pack(
         batch, cp, P, s_local, heads, d, direction, gather, _ptr(x), _ptr(out), _stream(stream)))
+
+
+def loong_headctx_pack_n(xs, outs, batch, cp, P, s_local, heads, d, direction, gather, stream=None):
+    """loong_headctx_pack over the tensors xs -> outs (up to 4), heads[t] heads each, one launch."""
+    n = len(xs)
+    hs = (ctypes.c_int32 * n)(*heads)
+    ins = (ctypes.c_void_p * n)(*[t.data_ptr() for t in xs])
+    ous = (ctypes.c_void_p * n)(*[t.data_ptr() for t in outs])
+    return _check("loong_headctx_pack_n", lib().loong_headctx_pack_n(
+        n, batch, cp, P, s_local, hs, d, direction, gather, ins, ous, _stream(stream)))
 
 
 def loong_attn_2d_host_workspace_size(desc, pass_):

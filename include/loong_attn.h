@@ -284,6 +284,18 @@ LOONG_API int loong_headctx_pack(int64_t batch, int32_t cp, int32_t P, int64_t s
                        loong_stream_t stream);
 
 /*
+ * loong_headctx_pack over n tensors (1 <= n <= 4) in one launch: the same
+ * batch, cp, P, s_local, d, direction and gather, their own head counts, as
+ * the Q, K, V (and dO) of one pass, whose repacks are the one all-to-all the
+ * guide describes.  Tensor t has heads[t] heads (each a multiple of P) and
+ * moves from in[t] to out[t]; heads, in and out are host arrays of n entries.
+ * The results equal n calls of loong_headctx_pack bit for bit.
+ */
+LOONG_API int loong_headctx_pack_n(int32_t n, int64_t batch, int32_t cp, int32_t P, int64_t s_local,
+                                   const int32_t* heads, int32_t d, int direction, int gather,
+                                   const void* const* in, void* const* out, loong_stream_t stream);
+
+/*
  * Device workspace, in bytes, of loong_attn_2d_host for `desc`: pass 0 runs
  * the forward alone, pass 1 the forward and the backward; 0 for an invalid
  * descriptor.  Host-only.  It holds two sets of natural-layout inputs (the

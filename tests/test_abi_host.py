@@ -201,3 +201,25 @@ def test_2d_host_validation_before_any_cuda_call(loong_lib):
     assert call(0, p, (p, p, p), ctypes.c_void_p((1 << 20) + 16), need) == ops.LOONG_ERR_WORKSPACE  # alignment
     assert L.loong_attn_2d_host(ctypes.byref(d), 0, None, p, p, p, p, p, p, p, p, ws, need, None, None) == \
         ops.LOONG_ERR_INVALID_ARG
+
+
+def test_headctx_pack_n_validation_before_any_cuda_call(loong_lib):
+    L = ops.lib()
+    P_ = ctypes.c_void_p
+    heads = (ctypes.c_int32 * 4)(8, 2, 2, 8)
+    bad_heads = (ctypes.c_int32 * 2)(8, 3)
+    ptrs = (P_ * 4)(16, 32, 48, 64)   # never dereferenced
+    nul = (P_ * 4)(16, None, 48, 64)
+    call = lambda n, h, i, o, d=128, direction=0, gather=1: L.loong_headctx_pack_n(
+        n, 1, 4, 2, 128, h, d, direction, gather, i, o, None)
+    for n in (0, 5, -1):
+        assert call(n, heads, ptrs, ptrs) == ops.LOONG_ERR_INVALID_ARG
+    assert call(2, bad_heads, ptrs, ptrs) == ops.LOONG_ERR_INVALID_ARG        # heads % P
+    assert call(4, heads, nul, ptrs) == ops.LOONG_ERR_INVALID_ARG             # a null tensor
+    assert call(4, None, ptrs, ptrs) == ops.LOONG_ERR_INVALID_ARG             # no head array
+    assert call(4, heads, ptrs, ptrs, d=4) == ops.LOONG_ERR_INVALID_ARG       # d*2 not a multiple of 16
+    assert call(4, heads, ptrs, ptrs, direction=2) == ops.LOONG_ERR_INVALID_ARG
+    assert call(4, heads, ptrs, ptrs, gather=3) == ops.LOONG_ERR_INVALID_ARG
+    mis = (P_ * 4)(16, 40, 48, 64)                                            # 8-byte aligned only
+    assert call(4, heads, mis, ptrs) == ops.LOONG_ERR_INVALID_ARG
+    assert L.loong_headctx_pack_n(4, 0, 4, 2, 128, heads, 128, 0, 1, ptrs, ptrs, None) == ops.LOONG_OK  # empty

@@ -72,3 +72,28 @@ def test_headctx_pack_rank_major_input(cuda_device):
     back = torch.empty_like(x)
     ops.loong_headctx_pack(out, back, n, 1, P, sl, H, d, 1, 0)
     assert torch.equal(back, x)
+
+
+@pytest.mark.parametrize("B,S,heads,d,cp,P,gather", [
+    (1, 1024, (8, 2, 2, 8), 128, 4, 2, 1), (1, 2048, (32, 8, 8), 128, 4, 4, 1), (2, 768, (6, 2), 64, 3, 2, 2),
+    (1, 512, (4,), 128, 2, 2, 1), (3, 384, (12, 3, 3, 12), 64, 2, 3, 2), (1, 4096, (64, 8, 8, 64), 128, 8, 8, 1)])
+def test_headctx_pack_n_equals_separate_packs(cuda_device, B, S, heads, d, cp, P, gather):
+    """One launch over up to four tensors with their own head counts gives what
+    separate loong_headctx_pack calls give, bit for bit, in both directions; the
+    first tensor is also checked against the oracle's repack."""
+    g = torch.Generator(device="cuda").manual_seed(S + sum(heads))
+    xs = [torch.randn((B, S, h, d), generator=g, device="cuda").to(torch.bfloat16) for h in heads]
+    s_local = S // (cp * P)
+    ys = [torch.full((B * cp, P, S // cp, h // P, d), 3.0, dtype=torch.bfloat16, device="cuda") for h in heads]
+    ops.loong_headctx_pack_n(xs, ys, B, cp, P, s_local, heads, d, 0, gather)
+    for x, y in zip(xs, ys):
+        assert torch.equal(y.view(torch.int16), ops.headctx_pack(x, cp, P, gather).view(torch.int16))
+    placement = 1 if gather == 1 else 0
+    xv = xs[0].view(torch.int16).cpu().numpy()
+    want = np.concatenate([repack.headctx_pack(xv[b], cp, P, placement) for b in range(B)])
+    assert np.array_equal(ys[0].view(torch.int16).cpu().numpy(), want)
+    backs = [torch.full_like(x, 5.0) for x in xs]
+    ops.loong_headctx_pack_n(ys, backs, B, cp, P, s_local, heads, d, 1, gather)
+    for x, back in zip(xs, backs):
+        assert torch.equal(back.view(torch.int16), x.view(torch.int16))
+    assert ops.loong_get_device_status() == ops.LOONG_OK
