@@ -22,14 +22,16 @@
 // plane of the rank that holds it at the launch's step (exchange.h), while dK
 // and dV go to the owner's rows.
 //
-// Warp roles (352 threads): warps 0-3 and 4-7 form two groups that each cover
-// all 128 TMEM lanes; group w handles query columns [64w, 64w+64) of S^T/dP^T
-// and head-dim columns [D/2*w, D/2*(w+1)) of dQ; warp 8 issues TMA loads,
-// warp 9 allocates TMEM and issues the MMAs, warp 10 issues the dQ bulk
-// reductions (so no compute warp waits on their completion).
+// Warp roles: compute warps form groups of four that each cover all 128 TMEM
+// lanes, two groups at d = 128 (352 threads) and four at d = 64 (608); group g
+// handles query columns [GW g, GW (g+1)) of S^T/dP^T and head-dim columns
+// [GD g, GD (g+1)) of dQ, and folds a share of dV (first half of the groups)
+// or dK (second half).  After them, one warp issues TMA loads, one allocates
+// TMEM and issues the MMAs, one issues the dQ bulk reductions (so no compute
+// warp waits on their completion).
 // Tensor memory (512 columns): R0 [0,128) S^T, then P^T as bf16 pairs, each
-// group packing its 64 queries into the first 32 columns of its own half (the
-// two groups share lanes, so neither may write where the other still reads);
+// group packing its GW queries into the first GW/2 columns of its own GW (the
+// groups share lanes, so none may write where another still reads);
 // R1 [128,256) dP^T then dQ; dV and dK after that (D columns each).
 #include <cuda_bf16.h>
 
@@ -55,7 +57,17 @@ struct BwdCfg {
   // Tiles first (1024-byte aligned, checked at run time), then the row
   // statistics stages, the barriers, the TMEM base address and the abort flag.
   static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16;
-  static constexpr int THREADS = 352;
+  // Compute groups of four warps, each covering all 128 TMEM lanes: group g
+  // owns query columns [GW g, GW (g+1)) of S^T / dP^T and head-dim columns
+  // [GD g, GD (g+1)) of dQ.  d = 64 has four (its per-iteration work is the
+  // compute warps' chain, which more warps overlap), d = 128 two.
+  static constexpr int GROUPS = D == 64 ? 4 : 2;
+  static constexpr int GW = kTile / GROUPS;  // query columns per group
+  static constexpr int GCH = GW / 32;        // 32-column chunks per group
+  static constexpr int GD = D / GROUPS;      // dQ head-dim columns per group
+  static constexpr int ACC_COLS = 2 * D / GROUPS;  // dV / dK columns each group folds
+  static constexpr int CW = 4 * GROUPS;      // compute warps; then producer, MMA, reducer
+  static constexpr int THREADS = 32 * (CW + 3);
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t R0 = 0, R1 = 128, RV = 256, RK = 256 + D;
   // dQ leaves through TMA bulk reductions of 32-float x 128-row boxes; the
@@ -69,6 +81,8 @@ struct BwdCfg {
   // both groups stage after dK(i) and the reducer takes the whole tile at once
   // (measured faster there).
   static constexpr bool EARLY_O = D == 64;
+  // groups whose dQ columns lie in the Q half of the stage (the rest: the dO half)
+  static constexpr int QHALF_GROUPS = BOXES_PER_STAGE * 32 / GD;
 };
 
 // dK and dV build up in tensor memory; every kFlush iterations they are added
@@ -98,7 +112,7 @@ struct BwdArgs {
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, bool STEP>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     ring_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdArgs a) {
@@ -167,27 +181,27 @@ __global__ void __launch_bounds__(352, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 8);
-    mbar_init(ds_full, 8);
+    mbar_init(p_full, C::CW);
+    mbar_init(ds_full, C::CW);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 8);
+    mbar_init(dq_empty, C::CW);
     mbar_init(dk_done, 1);
     for (int st = 0; st < C::NS; ++st) {
-      mbar_init(&staged_q[st], C::EARLY_O ? 4 : 8);
-      mbar_init(&staged_o[st], 4);
+      mbar_init(&staged_q[st], C::EARLY_O ? 4 * C::QHALF_GROUPS : C::CW);
+      mbar_init(&staged_o[st], 4 * (C::GROUPS - C::QHALF_GROUPS));
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 8);
+    mbar_init(acc_empty, C::CW);
     mbar_init(done_bar, 1);
     mbar_init(drain, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == C::CW + 1) {
     tmem_alloc(&tmem_base_sh, C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == C::CW && lane == 0) {
     tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
     tma_prefetch_map(&tmV);
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(352, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_base_sh;
 
-  if (warp == 8) {
+  if (warp == C::CW) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(kv_full, 2 * C::TILE_BYTES);
@@ -250,7 +264,7 @@ __global__ void __launch_bounds__(352, 1)
         if (cnt) mbar_drain(&q_full[s], (cnt - 1) & 1, a.err);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::CW + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
@@ -280,11 +294,12 @@ __global__ void __launch_bounds__(352, 1)
           const uint32_t qs = q_addr + s * C::TILE_BYTES, os = o_addr + s * C::TILE_BYTES;
           if (!mbar_wait(p_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
-          // dV += P^T dO: A = P^T (TMEM, 8 columns per 16 queries; queries 64..127
-          // start at column 64), B = dO MN-major
+          // dV += P^T dO: A = P^T (TMEM: each group's bf16 pairs in the first
+          // columns of its own GW, 8 columns per 16 queries), B = dO MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tbase + C::RV, tbase + C::R0 + (kk >> 2) * 64 + (kk & 3) * 8,
+            mma_ts(tbase + C::RV,
+                   tbase + C::R0 + (kk * 16 / C::GW) * C::GW + ((kk * 16 % C::GW) / 32) * 16 + (kk & 1) * 8,
                    sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, !fresh || kk > 0);
           if (!mbar_wait(ds_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
@@ -330,7 +345,7 @@ __global__ void __launch_bounds__(352, 1)
       mma_commit(drain);
       mbar_drain(drain, 0, a.err);
     }
-  } else if (warp == 10) {
+  } else if (warp == C::CW + 2) {
     // ------------------------------------------------------------ dQ reducer
     // Adds each staged dQ tile into the fp32 accumulator with TMA bulk tensor
     // reductions and hands the stage back to the producer once it is read.
@@ -370,7 +385,7 @@ __global__ void __launch_bounds__(352, 1)
     }
   } else {
     // ------------------------------------------------------------ compute warps
-    const int grp = warp >> 2;  // query columns [64 grp, 64 grp + 64)
+    const int grp = warp >> 2;  // query columns [GW grp, GW grp + GW)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;  // key row in the pass, query row in the dQ drain
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
@@ -380,10 +395,12 @@ __global__ void __launch_bounds__(352, 1)
                                                         static_cast<int64_t>(a.batch) * a.S * a.hkv,
                                                 a.err);
     const int64_t krow = a.lay.vec(b, k0 + row, kvh, a.hkv);  // this key row's d-vector in K / dK / dV
-    // group 0 owns dV, group 1 owns dK (keys on lanes)
-    const uint32_t acc_col = grp == 0 ? C::RV : C::RK;
-    float* acc_glob = (grp == 0 ? a.dv_acc : a.dk_acc) + krow * D;
-    const float acc_mul = grp == 0 ? 1.f : a.scale;
+    // the first half of the groups own dV, the second dK (keys on lanes), ACC_COLS columns each
+    const bool owns_dv = grp < C::GROUPS / 2;
+    const int acc_part = C::GROUPS == 2 ? 0 : (owns_dv ? grp : grp - C::GROUPS / 2) * C::ACC_COLS;
+    const uint32_t acc_col = (owns_dv ? C::RV : C::RK) + acc_part;
+    float* acc_glob = (owns_dv ? a.dv_acc : a.dk_acc) + krow * D + acc_part;
+    const float acc_mul = owns_dv ? 1.f : a.scale;
     bool ok = true;
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
@@ -402,17 +419,16 @@ __global__ void __launch_bounds__(352, 1)
         break;
       }
       tc_fence_after();
-      float pv[2][32];
+      float pv[C::GCH][32];
       {
-        uint32_t sv0[32], sv1[32];
-        tmem_ld32(tbase + t_lane + C::R0 + grp * 64, sv0);
-        tmem_ld32(tbase + t_lane + C::R0 + grp * 64 + 32, sv1);
+        uint32_t sv[C::GCH][32];
+#pragma unroll
+        for (int ch = 0; ch < C::GCH; ++ch) tmem_ld32(tbase + t_lane + C::R0 + grp * C::GW + ch * 32, sv[ch]);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          pv[0][e] = __uint_as_float(sv0[e]);
-          pv[1][e] = __uint_as_float(sv1[e]);
-        }
+        for (int ch = 0; ch < C::GCH; ++ch)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pv[ch][e] = __uint_as_float(sv[ch][e]);
       }
       // Query columns c with lo <= c < hi are live for this key row (causal
       // diagonal, ragged query tile, key row past the block).  Interior tiles
@@ -421,8 +437,8 @@ __global__ void __launch_bounds__(352, 1)
       const int hi = key_ok ? qlen : 0;
       const bool unmasked = __all_sync(0xffffffffu, lo == 0 && hi == kTile);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int cbase = grp * 64 + ch * 32;  // first query column of the chunk
+      for (int ch = 0; ch < C::GCH; ++ch) {
+        const int cbase = grp * C::GW + ch * 32;  // first query column of the chunk
         uint32_t pk[16];
         if (unmasked) {
 #pragma unroll
@@ -450,11 +466,11 @@ __global__ void __launch_bounds__(352, 1)
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 2) pk[e / 2] = pack_bf16(pv[ch][e], pv[ch][e + 1]);
-        // P^T (bf16 pairs) into this group's own half of R0, columns
-        // [64 grp + 16 ch, +16): already read by this group, never read by the other.
+        // P^T (bf16 pairs) into this group's own columns of R0,
+        // [GW grp + 16 ch, +16): already read by this group, never read by another.
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tbase + t_lane + C::R0 + grp * 64 + ch * 16),
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(tbase + t_lane + C::R0 + grp * C::GW + ch * 16),
             "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7]),
             "r"(pk[8]), "r"(pk[9]), "r"(pk[10]), "r"(pk[11]), "r"(pk[12]), "r"(pk[13]), "r"(pk[14]), "r"(pk[15])
             : "memory");
@@ -470,13 +486,13 @@ __global__ void __launch_bounds__(352, 1)
         break;
       }
       tc_fence_after();
-      uint32_t dpv2[2][32];
-      tmem_ld32(tbase + t_lane + C::R1 + grp * 64, dpv2[0]);
-      tmem_ld32(tbase + t_lane + C::R1 + grp * 64 + 32, dpv2[1]);
+      uint32_t dpv2[C::GCH][32];
+#pragma unroll
+      for (int ch = 0; ch < C::GCH; ++ch) tmem_ld32(tbase + t_lane + C::R1 + grp * C::GW + ch * 32, dpv2[ch]);
       tmem_wait_ld();
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        const int cbase = grp * 64 + ch * 32;
+      for (int ch = 0; ch < C::GCH; ++ch) {
+        const int cbase = grp * C::GW + ch * 32;
         const uint32_t(&dpv)[32] = dpv2[ch];
         uint32_t dsk[16];
 #pragma unroll
@@ -495,11 +511,12 @@ __global__ void __launch_bounds__(352, 1)
           dsk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
         }
         // dS^T row `row`, queries [cbase, cbase+32): 4 of the 8 16-byte units of
-        // this group's 128-byte line in atom `grp`, 128-byte swizzled.
-        uint8_t* line = sdS + grp * C::ATOM_BYTES + row * 128;
+        // the row's 128-byte line in query atom cbase / 64, 128-byte swizzled
+        // (written so that GW = 64 folds to constants).
+        uint8_t* line = sdS + (grp * C::GW / 64) * C::ATOM_BYTES + row * 128;
 #pragma unroll
         for (int uu = 0; uu < 4; ++uu) {
-          const int unit = ch * 4 + uu;
+          const int unit = (grp * C::GW % 64) / 8 + ch * 4 + uu;
           uint4 w;
           w.x = dsk[uu * 4 + 0];
           w.y = dsk[uu * 4 + 1];
@@ -524,39 +541,51 @@ __global__ void __launch_bounds__(352, 1)
       tc_fence_after();
       {
         const bool q_ok = row < qlen;
-        uint32_t qv[D / 64][32];
+        // this group's GD columns of dQ in runs of RUN (one TMEM load each)
+        constexpr int RUN = C::GD >= 32 ? 32 : 16;
+        constexpr int NR = C::GD / RUN;
+        uint32_t qv[NR][RUN];
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb) tmem_ld32(tbase + t_lane + C::R1 + grp * (D / 2) + cb * 32, qv[cb]);
+        for (int cb = 0; cb < NR; ++cb) {
+          if constexpr (RUN == 32)
+            tmem_ld32(tbase + t_lane + C::R1 + grp * C::GD + cb * RUN, qv[cb]);
+          else
+            tmem_ld16(tbase + t_lane + C::R1 + grp * C::GD + cb * RUN, qv[cb]);
+        }
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dq_empty);
-        // group 0 stages into the Q half, which dK(i) may still read; group 1
-        // into the dO half, whose last reader dV(i) retired before dQ(i)
-        if ((grp == 0 || !C::EARLY_O) && !warp_wait(dk_done, i & 1)) {
+        // groups staging into the Q half wait for dK(i), which may still read
+        // it; the others write the dO half, whose last reader dV(i) retired
+        // before dQ(i)
+        const bool q_half = grp < C::QHALF_GROUPS || !C::EARLY_O;
+        if (q_half && !warp_wait(dk_done, i & 1)) {
           ok = false;
           break;
         }
         const int s = i % C::NS;
 #pragma unroll
-        for (int cb = 0; cb < D / 64; ++cb) {
-          const int box = grp * (D / 64) + cb;
+        for (int cb = 0; cb < NR; ++cb) {
+          const int col = grp * C::GD + cb * RUN;  // first dQ column of the run
+          const int box = col / 32;
           uint8_t* base = box < C::BOXES_PER_STAGE ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
                                                    : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
           uint8_t* line = base + row * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < RUN / 4; ++c) {
+            const int unit = (col % 32) / 4 + c;
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             if (q_ok)
               x = make_float4(__uint_as_float(qv[cb][c * 4]) * a.scale, __uint_as_float(qv[cb][c * 4 + 1]) * a.scale,
                               __uint_as_float(qv[cb][c * 4 + 2]) * a.scale,
                               __uint_as_float(qv[cb][c * 4 + 3]) * a.scale);
-            *reinterpret_cast<float4*>(line + ((c ^ (row & 7)) << 4)) = x;
+            *reinterpret_cast<float4*>(line + ((unit ^ (row & 7)) << 4)) = x;
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(grp == 0 || !C::EARLY_O ? &staged_q[s] : &staged_o[s]);
+        if (lane == 0) mbar_arrive(q_half ? &staged_q[s] : &staged_o[s]);
       }
 
       // ---- every kFlush iterations: fold dV / dK into the fp32 accumulators
@@ -567,7 +596,7 @@ __global__ void __launch_bounds__(352, 1)
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
+        for (int cb = 0; cb < C::ACC_COLS / 32; ++cb) {
           uint32_t v[32];
           tmem_ld32(tbase + t_lane + acc_col + cb * 32, v);
           tmem_wait_ld();
@@ -596,7 +625,7 @@ __global__ void __launch_bounds__(352, 1)
       // the accumulator holds earlier flushes (FUSED) or earlier steps (STEPWISE)
       const bool add_glob = STEP || nflush > 0;
 #pragma unroll 1
-      for (int cb = 0; cb < D / 32; ++cb) {
+      for (int cb = 0; cb < C::ACC_COLS / 32; ++cb) {
         uint32_t v[32];
         tmem_ld32(tbase + t_lane + acc_col + cb * 32, v);
         tmem_wait_ld();
@@ -616,7 +645,7 @@ __global__ void __launch_bounds__(352, 1)
             }
           }
           if constexpr (!STEP) {
-            __nv_bfloat16* dst = (grp == 0 ? a.dv : a.dk) + krow * D + cb * 32;
+            __nv_bfloat16* dst = (owns_dv ? a.dv : a.dk) + krow * D + acc_part + cb * 32;
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 w;
@@ -639,7 +668,7 @@ __global__ void __launch_bounds__(352, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::CW + 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
   }
