@@ -22,8 +22,8 @@
 // plane of the rank that holds it at the launch's step (exchange.h), while dK
 // and dV go to the owner's rows.
 //
-// Warp roles: compute warps form groups of four that each cover all 128 TMEM
-// lanes, two groups at d = 128 (352 threads) and four at d = 64 (608); group g
+// Warp roles: compute warps form four groups of four warps that each cover all
+// 128 TMEM lanes (608 threads with the three below); group g
 // handles query columns [GW g, GW (g+1)) of S^T/dP^T and head-dim columns
 // [GD g, GD (g+1)) of dQ, and folds a share of dV (first half of the groups)
 // or dK (second half).  After them, one warp issues TMA loads, one allocates
@@ -59,9 +59,13 @@ struct BwdCfg {
   static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16;
   // Compute groups of four warps, each covering all 128 TMEM lanes: group g
   // owns query columns [GW g, GW (g+1)) of S^T / dP^T and head-dim columns
-  // [GD g, GD (g+1)) of dQ.  d = 64 has four (its per-iteration work is the
-  // compute warps' chain, which more warps overlap), d = 128 two.
-  static constexpr int GROUPS = D == 64 ? 4 : 2;
+  // [GD g, GD (g+1)) of dQ.  Four groups (four compute warps per scheduler)
+  // overlap the compute warps' chain of TMEM loads, exponentials and stores
+  // better than two (measured faster at d = 64 and d = 128).
+#ifndef LOONG_BWD_GROUPS
+#define LOONG_BWD_GROUPS 4
+#endif
+  static constexpr int GROUPS = LOONG_BWD_GROUPS;
   static constexpr int GW = kTile / GROUPS;  // query columns per group
   static constexpr int GCH = GW / 32;        // 32-column chunks per group
   static constexpr int GD = D / GROUPS;      // dQ head-dim columns per group
@@ -75,12 +79,11 @@ struct BwdCfg {
   static constexpr int DQ_BOXES = D / 32;
   static constexpr int BOX_BYTES = kTile * 128;
   static constexpr int BOXES_PER_STAGE = TILE_BYTES / BOX_BYTES;
-  // Group 1's dQ columns land in the dO half of the stage, which dV(i) has
-  // finished reading before dQ(i) exists.  At d = 64 group 1 stages them at
-  // once and the reducer adds that half first (measured faster); at d = 128
-  // both groups stage after dK(i) and the reducer takes the whole tile at once
-  // (measured faster there).
-  static constexpr bool EARLY_O = D == 64;
+  // The groups whose dQ columns land in the dO half of the stage stage them at
+  // once (dV(i), the last reader of that half, retired before dQ(i) exists)
+  // and the reducer adds that half first; the Q half waits for dK(i).
+  // Measured faster at both head dimensions with four compute groups.
+  static constexpr bool EARLY_O = true;
   // groups whose dQ columns lie in the Q half of the stage (the rest: the dO half)
   static constexpr int QHALF_GROUPS = BOXES_PER_STAGE * 32 / GD;
 };
@@ -145,8 +148,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* drain = done_bar + 1;
   // per stage, so that neither runs a phase ahead of the reducer: a stage is
   // staged into again only after the reducer has read it and it was reloaded
-  uint64_t* staged_q = drain + 1;       // NS: dQ(i) staged (EARLY_O: group 0's Q half)  (warps -> reducer)
-  uint64_t* staged_o = staged_q + C::NS;  // NS: EARLY_O: group 1's dO half             (warps -> reducer)
+  uint64_t* staged_q = drain + 1;       // NS: dQ(i) columns staged in the Q half (warps -> reducer)
+  uint64_t* staged_o = staged_q + C::NS;  // NS: dQ(i) columns staged in the dO half (warps -> reducer)
   uint32_t& tmem_base_sh = *reinterpret_cast<uint32_t*>(bars + C::NBARS);
   int& abort_sh = *(reinterpret_cast<int*>(bars + C::NBARS) + 1);
   volatile int* abort_flag = &abort_sh;
