@@ -159,3 +159,26 @@ def test_device_memory_in_host_arguments_is_refused(cuda_device):
     torch.cuda.synchronize()
     assert bool((hout["o"].float() == 7.0).all())   # nothing was enqueued
     assert ops.loong_get_device_status() == ops.LOONG_OK
+
+
+MODE_CASES = [
+    ("stepwise", inputs.small(2048, 8, 2, 128, hp=2, cp=4, inner=2, outer=2), ops.MODE_STEPWISE),
+    ("stepwise-copy", inputs.small(2048, 8, 2, 128, hp=2, cp=4, inner=2, outer=2), ops.MODE_STEPWISE_COPY),
+    ("non-causal batch 2", inputs.small(1024, 4, 2, 64, hp=2, cp=2, inner=2).with_(causal=False, batch=2),
+     ops.MODE_FUSED),
+]
+
+
+@pytest.mark.parametrize("name,w,mode", MODE_CASES, ids=[c[0] for c in MODE_CASES])
+def test_host_pass_other_modes_equal_device_pass(cuda_device, name, w, mode):
+    """The host pass passes the descriptor's mode, causality and batch through to
+    the ring kernels: its results equal the device entry points' in that mode."""
+    x = inputs.make_inputs(w, device="cuda")
+    desc = ops.make_desc(w, mode, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_check(desc) == ops.LOONG_OK
+    ws = torch.empty(ops.loong_attn_2d_host_workspace_size(desc, 1), dtype=torch.uint8, device="cuda")
+    hin, hout = _host_buffers(w, x)
+    _host_pass(desc, w, 0, hin, hout, ws)
+    torch.cuda.synchronize()
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    _check_equal(w, hout, _device_pass(w, x, ops.LAYOUT_RANK_MAJOR, mode))
