@@ -201,13 +201,14 @@ def time_per_rank(w, x, stream, dev, reps=3):
         desc = ops.make_desc(wp, ops.MODE_FUSED)
         if ops.loong_attn_check(desc) != ops.LOONG_OK:
             continue
+        ws = ops.workspace(desc, 0, dev)
         ms = []
         for c in range(w.cp):
-            ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, stream)
+            ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, ws, stream)
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
             for a, b in ev:
                 a.record(stream)
-                ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, stream)
+                ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, ws, stream)
                 b.record(stream)
             torch.cuda.synchronize(dev)
             ms.append(statistics.median(a.elapsed_time(b) for a, b in ev))
@@ -401,11 +402,18 @@ class TwoDPath:
         if self.rank_major:
             self.kt = {n: torch.empty((B * w.cp, w.hp, S // w.cp, h // w.hp, d), **bf) for n, h in nat.items()}
         self.do_bwd = w.backward
+        # the forward's rounding residual of O, kept on the device for the
+        # backward's D (in the layout the ring kernels use)
+        self.o_res = (torch.empty_like(self.kt["o"] if self.rank_major else self.out["o"])
+                      if self.do_bwd else None)
 
     def launches(self):
+        """Kernels of one step: forward = max |V| + V to fp16 + ring kernel(s)
+        (+ LSE fill and O conversion, STEPWISE); backward = row statistics +
+        ring kernel(s) + dQ conversion (+ dK, dV conversions, STEPWISE)."""
         ops, w = self.ops, self.w
         fused = self.desc.mode == ops.MODE_FUSED
-        n = (1 if fused else w.cp + 2) + (((3 if fused else w.cp + 4)) if self.do_bwd else 0)
+        n = (3 if fused else w.cp + 4) + (((3 if fused else w.cp + 4)) if self.do_bwd else 0)
         if self.rank_major:
             n += 2   # one repack launch in, one out
         return n
@@ -429,7 +437,7 @@ class TwoDPath:
     def fwd(self, x):
         t = self.kt if self.rank_major else x
         o = self.kt["o"] if self.rank_major else self.out["o"]
-        self.ops.loong_attn_fwd(self.desc, t["q"], t["k"], t["v"], o, self.lse, self.ws0, self.stream)
+        self.ops.loong_attn_fwd(self.desc, t["q"], t["k"], t["v"], o, self.lse, self.o_res, self.ws0, self.stream)
 
     def bwd(self, x):
         if not self.do_bwd:
@@ -437,8 +445,8 @@ class TwoDPath:
         t = self.kt if self.rank_major else x
         g = self.kt if self.rank_major else self.out
         o = self.kt["o"] if self.rank_major else self.out["o"]
-        self.ops.loong_attn_bwd(self.desc, t["q"], t["k"], t["v"], o, self.lse, t["do"], g["dq"], g["dk"],
-                                g["dv"], self.ws1, self.stream)
+        self.ops.loong_attn_bwd(self.desc, t["q"], t["k"], t["v"], o, self.o_res, self.lse, t["do"], g["dq"],
+                                g["dk"], g["dv"], self.ws1, self.stream)
 
     def unpack_out(self, names=None):
         """Repack the named outputs (default: every output of the pass) back to the natural layout."""

@@ -194,6 +194,35 @@ RingGeom ring_geom(const loong_attn_desc& d) {
   return g;
 }
 
+FwdWsLayout fwd_ws_layout(const loong_attn_desc& d) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t q_elems = static_cast<size_t>(d.batch) * d.seqlen * d.hq * d.head_dim;
+  const size_t kv_elems = static_cast<size_t>(d.batch) * d.seqlen * d.hkv * d.head_dim;
+  FwdWsLayout L{};
+  L.v16 = 0;
+  L.amax = up(kv_elems * 2);
+  size_t off = L.amax + 256;
+  L.o_acc = off;
+  if (d.mode != LOONG_MODE_FUSED) off += up(q_elems * 4);
+  L.recv = off;
+  if (is_copy_mode(d)) off += 4 * up(kv_elems * 2);  // two receive buffers each for K and V
+  L.total = off;
+  return L;
+}
+
+// The forward's scratch pointers inside a workspace of fwd_ws_layout(d).total bytes.
+static FwdScratch fwd_scratch(const loong_attn_desc& d, void* ws, void* o_res) {
+  const FwdWsLayout L = fwd_ws_layout(d);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  FwdScratch sc;
+  sc.v16 = w + L.v16;
+  sc.v_amax = reinterpret_cast<unsigned*>(w + L.amax);
+  sc.o_acc = d.mode != LOONG_MODE_FUSED ? reinterpret_cast<float*>(w + L.o_acc) : nullptr;
+  sc.kv_recv = is_copy_mode(d) ? w + L.recv : nullptr;
+  sc.o_res = o_res;
+  return sc;
+}
+
 Layout layout_of(const loong_attn_desc& d) {
   const RingGeom g = ring_geom(d);
   Layout l;
@@ -213,7 +242,7 @@ using namespace loong;
 
 extern "C" {
 
-int loong_version(void) { return (0 << 16) | 2; }
+int loong_version(void) { return (0 << 16) | 3; }
 
 const char* loong_status_string(int status) {
   switch (status) {
@@ -265,7 +294,7 @@ size_t loong_attn_workspace_size(const loong_attn_desc* d, int pass) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   // STEPWISE_COPY: two receive buffers each for K and V, bf16
   const size_t recv = is_copy_mode(*d) ? 4 * up(kv_elems * 2) : 0;
-  if (pass == 0) return d->mode == LOONG_MODE_FUSED ? 0 : up(q_elems * 4) + recv;
+  if (pass == 0) return fwd_ws_layout(*d).total;
   if (pass != 1) return 0;
   const size_t stats = 2 * static_cast<size_t>(d->batch) * d->hq * stat_row_len(ring_geom(*d));
   return up(q_elems * 4) + up(stats * 4) + 2 * up(kv_elems * 4) + recv;
@@ -281,32 +310,32 @@ int loong_ring_schedule(int32_t inner, int32_t outer, int32_t* src) {
 }
 
 int loong_attn_fwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, void* o,
-                   float* lse, void* ws, size_t ws_bytes, loong_stream_t stream_) {
+                   float* lse, void* o_res, void* ws, size_t ws_bytes, loong_stream_t stream_) {
   NvtxRange range("loong_attn_fwd");
   int st = loong_attn_check(d);
   if (st != LOONG_OK) return st;
   if (!q || !k || !v || !o || !lse) return LOONG_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (o_res && !aligned16(o_res)))
     return LOONG_ERR_INVALID_ARG;
   const size_t need = loong_attn_workspace_size(d, 0);
-  if (need && (!ws || ws_bytes < need || !aligned16(ws))) return LOONG_ERR_WORKSPACE;
+  if (!ws || ws_bytes < need || !aligned16(ws)) return LOONG_ERR_WORKSPACE;
   if ((st = device_ready()) != LOONG_OK) return st;
-  if (!all_on_device(q, k, v, o, lse) || (need && !on_device(ws))) return LOONG_ERR_INVALID_ARG;
+  if (!all_on_device(q, k, v, o, lse, ws) || (o_res && !on_device(o_res))) return LOONG_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (d->mode == LOONG_MODE_FUSED) return launch_fwd(*d, q, k, v, o, lse, nullptr, stream);
+  const FwdScratch sc = fwd_scratch(*d, ws, o_res);
+  if (d->mode == LOONG_MODE_FUSED) return launch_fwd(*d, q, k, v, o, lse, sc, stream);
   const int64_t q_elems = d->batch * d->seqlen * d->hq * d->head_dim;
-  float* o_acc = static_cast<float*>(ws);
-  cudaError_t e = cudaMemsetAsync(o_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
+  cudaError_t e = cudaMemsetAsync(sc.o_acc, 0, static_cast<size_t>(q_elems) * 4, stream);
   if (e != cudaSuccess) return cuda_fail(e);
   if ((st = launch_fill_f32(lse, d->batch * d->hq * d->seqlen, -INFINITY, stream)) != LOONG_OK) return st;
-  void* recv = is_copy_mode(*d) ? static_cast<uint8_t*>(ws) + ((q_elems * 4 + 255) & ~255LL)
-                                                   : nullptr;
-  if ((st = launch_fwd(*d, q, k, v, o, lse, o_acc, stream, 0, -1, recv)) != LOONG_OK) return st;
-  return launch_f32_to_bf16(o_acc, o, q_elems, stream);
+  if ((st = launch_fwd(*d, q, k, v, o, lse, sc, stream)) != LOONG_OK) return st;
+  return launch_f32_to_bf16(sc.o_acc, o, q_elems, stream, o_res);
 }
 
 int loong_attn_fwd_ranks(const loong_attn_desc* d, int32_t rank_begin, int32_t rank_end, const void* q,
-                         const void* k, const void* v, void* o, float* lse, loong_stream_t stream_) {
+                         const void* k, const void* v, void* o, float* lse, void* ws, size_t ws_bytes,
+                         loong_stream_t stream_) {
   NvtxRange range("loong_attn_fwd_ranks");
   int st = loong_attn_check(d);
   if (st != LOONG_OK) return st;
@@ -315,13 +344,15 @@ int loong_attn_fwd_ranks(const loong_attn_desc* d, int32_t rank_begin, int32_t r
   if (!q || !k || !v || !o || !lse) return LOONG_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return LOONG_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < loong_attn_workspace_size(d, 0) || !aligned16(ws)) return LOONG_ERR_WORKSPACE;
   if ((st = device_ready()) != LOONG_OK) return st;
-  if (!all_on_device(q, k, v, o, lse)) return LOONG_ERR_INVALID_ARG;
-  return launch_fwd(*d, q, k, v, o, lse, nullptr, reinterpret_cast<cudaStream_t>(stream_), rank_begin, rank_end);
+  if (!all_on_device(q, k, v, o, lse, ws)) return LOONG_ERR_INVALID_ARG;
+  return launch_fwd(*d, q, k, v, o, lse, fwd_scratch(*d, ws, nullptr), reinterpret_cast<cudaStream_t>(stream_),
+                    rank_begin, rank_end);
 }
 
 int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const void* v, const void* o,
-                   const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
+                   const void* o_res, const float* lse, const void* dout, void* dq, void* dk, void* dv, void* ws,
                    size_t ws_bytes, loong_stream_t stream_) {
   NvtxRange range("loong_attn_bwd");
   int st = loong_attn_check(d);
@@ -330,12 +361,13 @@ int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const
   const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv};
   for (const void* p : ptrs)
     if (!aligned16(p)) return LOONG_ERR_INVALID_ARG;
+  if (o_res && !aligned16(o_res)) return LOONG_ERR_INVALID_ARG;
   const size_t need = loong_attn_workspace_size(d, 1);
   if (!ws || ws_bytes < need || !aligned16(ws)) return LOONG_ERR_WORKSPACE;
   if ((st = device_ready()) != LOONG_OK) return st;
   for (const void* p : ptrs)
     if (!on_device(p)) return LOONG_ERR_INVALID_ARG;
-  if (!on_device(ws)) return LOONG_ERR_INVALID_ARG;
+  if (!on_device(ws) || (o_res && !on_device(o_res))) return LOONG_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t q_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hq * d->head_dim;
@@ -347,7 +379,7 @@ int loong_attn_bwd(const loong_attn_desc* d, const void* q, const void* k, const
   float* dk_acc = reinterpret_cast<float*>(w + up(q_elems * 4) + up(stats * 4));
   float* dv_acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dk_acc) + up(kv_elems * 4));
   void* recv = is_copy_mode(*d) ? reinterpret_cast<uint8_t*>(dv_acc) + up(kv_elems * 4) : nullptr;
-  return launch_bwd(*d, q, k, v, o, lse, dout, dq, dk, dv, dq_acc, dvec, dk_acc, dv_acc, stream, recv);
+  return launch_bwd(*d, q, k, v, o, o_res, lse, dout, dq, dk, dv, dq_acc, dvec, dk_acc, dv_acc, stream, recv);
 }
 
 int loong_lse_merge(int64_t rows, int32_t d, int32_t n_parts, const float* o_parts, const float* lse_parts,

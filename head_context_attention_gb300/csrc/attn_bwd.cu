@@ -769,7 +769,7 @@ int launch_bwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
 }  // namespace
 
 int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, const void* o,
-               const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dq_acc, float* dvec,
+               const void* o_res, const float* lse, const void* dout, void* dq, void* dk, void* dv, float* dq_acc, float* dvec,
                float* dk_acc, float* dv_acc, cudaStream_t stream, void* kv_recv) {
   const int64_t q_elems = d.batch * d.seqlen * d.hq * d.head_dim;
   const int64_t kv_elems = d.batch * d.seqlen * d.hkv * d.head_dim;
@@ -780,7 +780,7 @@ int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const voi
   if ((e = cudaMemsetAsync(dk_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess ||
       (e = cudaMemsetAsync(dv_acc, 0, static_cast<size_t>(kv_elems) * 4, stream)) != cudaSuccess)
     return cuda_fail(e);
-  if ((st = launch_bwd_rowstats(d, o, dout, lse, dvec, stream)) != LOONG_OK) return st;
+  if ((st = launch_bwd_rowstats(d, o, o_res, dout, lse, dvec, stream)) != LOONG_OK) return st;
   if (d.head_dim == 128)
     st = step ? launch_bwd_t<128, true>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream, kv_recv)
               : launch_bwd_t<128, false>(d, q, k, v, dout, dvec, dq_acc, dk, dv, dk_acc, dv_acc, stream, kv_recv);

@@ -6,7 +6,14 @@
 //   S_h = Q_h K_j^T                 tcgen05.mma, operands in shared memory
 //   P_h = exp2(S_h*scale*log2e - m) softmax warps, one thread per query row
 //   O_h += P_h V_j                  tcgen05.mma, P from tensor memory
-// with a running row maximum m and row sum l.  The per-step "merge" of
+// with a running row maximum m and row sum l.  The P V product takes fp16
+// operands: P as fp16 (scaled by 2^7, so that the largest probability, at most
+// 2^8 relative to the running maximum, sits near the top of fp16's range and
+// small ones stay clear of its subnormals) and V as the fp16 copy V * 2^-e the
+// launcher prepares (v16_shift); the epilogue removes both scalings exactly.
+// fp16's 11 significant bits keep O within about 2^-12 of its exact value,
+// which lets the backward form D = rowsum(dO * O) from O and its rounding
+// residual (o_res) to that precision.  The per-step "merge" of
 // [G] "Guide to LoongTrain", "Step 3" (partial results of successive ring
 // steps) is the online-softmax update itself: O and l carry the reference
 // maximum m, and a step whose maximum exceeds m by more than 2^8 rescales O
@@ -23,7 +30,7 @@
 // head slot 1 (warp w reads TMEM lanes 32*(w%4)..+31, the rows it owns),
 // warp 8 issues TMA loads, warp 9 allocates TMEM and issues the MMAs.
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
-// that (d columns each).  P_h overwrites the first 64 columns of S_h as bf16
+// that (d columns each).  P_h overwrites the first 64 columns of S_h as fp16
 // pairs; the next Q K^T into S_h is issued after O_h += P_h V and tcgen05
 // operations issued by one thread execute in order.
 #include <cuda_bf16.h>
@@ -62,18 +69,19 @@ struct FwdArgs {
   int t_begin, t_end;
   float scale_log2;
   __nv_bfloat16* o;
+  __nv_bfloat16* o_res;    // FUSED: bf16 rounding residual of O, or null
   float* lse;
-  float* o_acc;  // STEPWISE accumulator, else null
+  float* o_acc;            // STEPWISE accumulator, else null
+  const unsigned* v_amax;  // bit pattern of max |V|: V was stored as V * 2^-v16_shift
   unsigned* err;
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-// Of every 8 consecutive score columns, this many take their exponential on
-// the FMA pipe (exp2_fma) instead of the MUFU unit.
-template <int D>
-constexpr int kFmaExpPer8 = 0;
+// P is formed as exp2(x + kPBias): with the lazy rescale every probability is at
+// most 2^8 relative to the running maximum, so fp16 P stays below 2^15.
+constexpr float kPBias = 7.0f;
 
 template <int D, bool STEP>
 __global__ void __launch_bounds__(320, 1)
@@ -210,7 +218,7 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t id_pv = idesc_bf16(128, D, false, true);
+      constexpr uint32_t id_pv = idesc_f16(128, D, false, true);  // P and V in fp16
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
       auto qk = [&](int h, int s) {
 #pragma unroll
@@ -331,9 +339,10 @@ __global__ void __launch_bounds__(320, 1)
         if (rescale) m_run = m_new;
       }
       const float ref = m_run == -INFINITY ? 0.f : m_run;
-      // column pairs on the paired fp32 pipe: x = s*scale*log2e - m, and the
-      // two running sums (each half rounds as the scalar operation would)
-      const float2 sl2v = make_float2(sl2, sl2), nref = make_float2(-ref, -ref);
+      // column pairs on the paired fp32 pipe: x = s*scale*log2e - m + bias, and
+      // the two running sums (each half rounds as the scalar operation would);
+      // l carries the factor 2^bias as well
+      const float2 sl2v = make_float2(sl2, sl2), nref = make_float2(kPBias - ref, kPBias - ref);
       float2 lsum = make_float2(0.f, 0.f);
       uint32_t pk[2][32];
 #pragma unroll
@@ -342,10 +351,10 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 32; i += 2) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1])),
                                       sl2v, nref);
-          const float p0 = (i & 7) < kFmaExpPer8<D> ? exp2_fma(x.x) : fast_exp2(x.x);
-          const float p1 = ((i + 1) & 7) < kFmaExpPer8<D> ? exp2_fma(x.y) : fast_exp2(x.y);
+          const float p0 = fast_exp2(x.x);
+          const float p1 = fast_exp2(x.y);
           lsum = __fadd2_rn(lsum, make_float2(p0, p1));
-          pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_bf16(p0, p1);
+          pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_f16(p0, p1);
         }
       l_run += lsum.x + lsum.y;
       tmem_st32(tS, pk[0]);
@@ -367,26 +376,48 @@ __global__ void __launch_bounds__(320, 1)
                          in_bounds(qv >= 0 && qv < static_cast<int64_t>(a.batch) * a.S * a.hq && lse_i >= 0 &&
                                        lse_i < static_cast<int64_t>(a.batch) * a.hq * a.S,
                                    a.err);
-      const float lse_p = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      // l_run and O carry 2^kPBias; O also carries V's 2^-e
+      const float lse_p = l_run > 0.f ? (m_run + log2f(l_run) - kPBias) * kLn2 : -INFINITY;
+      const float o_mul = __int_as_float((127 + v16_shift(*a.v_amax)) << 23);  // 2^e
       float* lse_ptr = a.lse + lse_i;
       if constexpr (!STEP) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv = l_run > 0.f ? o_mul / l_run : 0.f;
         __nv_bfloat16* orow = a.o + qv * D;
+        __nv_bfloat16* rrow = a.o_res ? a.o_res + qv * D : nullptr;
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
           uint32_t ov[32];
           tmem_ld32(tO + cb * 32, ov);
           tmem_wait_ld();
           if (valid) {
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(ov[e]) * inv;
             uint4* dst = reinterpret_cast<uint4*>(orow + cb * 32);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 w;
-              w.x = pack_bf16(__uint_as_float(ov[v4 * 8 + 0]) * inv, __uint_as_float(ov[v4 * 8 + 1]) * inv);
-              w.y = pack_bf16(__uint_as_float(ov[v4 * 8 + 2]) * inv, __uint_as_float(ov[v4 * 8 + 3]) * inv);
-              w.z = pack_bf16(__uint_as_float(ov[v4 * 8 + 4]) * inv, __uint_as_float(ov[v4 * 8 + 5]) * inv);
-              w.w = pack_bf16(__uint_as_float(ov[v4 * 8 + 6]) * inv, __uint_as_float(ov[v4 * 8 + 7]) * inv);
+              w.x = pack_bf16(x[v4 * 8 + 0], x[v4 * 8 + 1]);
+              w.y = pack_bf16(x[v4 * 8 + 2], x[v4 * 8 + 3]);
+              w.z = pack_bf16(x[v4 * 8 + 4], x[v4 * 8 + 5]);
+              w.w = pack_bf16(x[v4 * 8 + 6], x[v4 * 8 + 7]);
               dst[v4] = w;
+            }
+            if (rrow) {
+              // x - bf16(x) is exact in fp32; rounded once more to bf16 it
+              // carries the next 8 bits of O
+              uint4* rdst = reinterpret_cast<uint4*>(rrow + cb * 32);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) {
+                uint32_t r[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float a0 = x[v4 * 8 + 2 * u], a1 = x[v4 * 8 + 2 * u + 1];
+                  r[u] = pack_bf16(a0 - __bfloat162float(__float2bfloat16_rn(a0)),
+                                   a1 - __bfloat162float(__float2bfloat16_rn(a1)));
+                }
+                rdst[v4] = make_uint4(r[0], r[1], r[2], r[3]);
+              }
             }
           }
         }
@@ -402,7 +433,7 @@ __global__ void __launch_bounds__(320, 1)
           const float tot = wa + wp;
           if (tot > 0.f) {
             ca = wa / tot;
-            cpart = wp / (tot * l_run);
+            cpart = wp * o_mul / (tot * l_run);
             lse_new = mm + log2f(tot) * kLn2;
           }
         }
@@ -439,16 +470,19 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 template <int D, bool STEP>
-int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-                 float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end, void* kv_recv) {
+int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, void* o,
+                 float* lse, const FwdScratch& sc, cudaStream_t stream, int rank_begin, int rank_end) {
   using C = FwdCfg<D>;
   const Layout lay = layout_of(d);
   const int64_t rows = lay.view_rows(d.batch);
   CUtensorMap mq, mk, mv;
   int st;
+  // V is read as its fp16 copy (the map moves 2-byte elements either way)
+  const void* v = sc.v16;
   if ((st = make_head_tile_map(&mq, q, rows, lay.view_heads(d.hq), D)) != LOONG_OK) return st;
   if ((st = make_head_tile_map(&mk, k, rows, lay.view_heads(d.hkv), D)) != LOONG_OK) return st;
   if ((st = make_head_tile_map(&mv, v, rows, lay.view_heads(d.hkv), D)) != LOONG_OK) return st;
+  void* kv_recv = sc.kv_recv;
 
   FwdArgs a;
   a.batch = static_cast<int>(d.batch);
@@ -465,8 +499,10 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
   const float scale = d.softmax_scale > 0.f ? d.softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = scale * kLog2e;
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.o_res = static_cast<__nv_bfloat16*>(sc.o_res);
   a.lse = lse;
-  a.o_acc = o_acc;
+  a.o_acc = sc.o_acc;
+  a.v_amax = sc.v_amax;
   a.err = device_error_word();
   if (!a.err) return LOONG_ERR_CUDA;
 
@@ -523,15 +559,18 @@ int launch_fwd_t(const loong_attn_desc& d, const void* q, const void* k, const v
 }  // namespace
 
 int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-               float* lse, float* o_acc, cudaStream_t stream, int rank_begin, int rank_end, void* kv_recv) {
+               float* lse, const FwdScratch& sc, cudaStream_t stream, int rank_begin, int rank_end) {
   const bool step = d.mode != LOONG_MODE_FUSED;
   if (rank_end < 0) rank_end = d.cp;
+  int st;
+  if ((st = launch_v_to_f16(v, sc.v16, sc.v_amax, d.batch * d.seqlen * d.hkv * d.head_dim, stream)) != LOONG_OK)
+    return st;
   if (d.head_dim == 128)
-    return step ? launch_fwd_t<128, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv)
-                : launch_fwd_t<128, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv);
+    return step ? launch_fwd_t<128, true>(d, q, k, o, lse, sc, stream, rank_begin, rank_end)
+                : launch_fwd_t<128, false>(d, q, k, o, lse, sc, stream, rank_begin, rank_end);
   if (d.head_dim == 64)
-    return step ? launch_fwd_t<64, true>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv)
-                : launch_fwd_t<64, false>(d, q, k, v, o, lse, o_acc, stream, rank_begin, rank_end, kv_recv);
+    return step ? launch_fwd_t<64, true>(d, q, k, o, lse, sc, stream, rank_begin, rank_end)
+                : launch_fwd_t<64, false>(d, q, k, o, lse, sc, stream, rank_begin, rank_end);
   return LOONG_ERR_UNSUPPORTED;
 }
 

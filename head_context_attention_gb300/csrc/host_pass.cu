@@ -72,6 +72,7 @@ struct HostPassLayout {
   size_t in[2][4];    // slot inputs q, k, v, dO (natural layout)
   size_t out[4];      // natural outputs o, dq, dk, dv
   size_t lse_off;
+  size_t ores;        // the forward's residual of O (pass 1), in the layout the kernels use
   size_t kt[8];       // RANK_MAJOR: q, k, v, dO, o, dq, dk, dv
   size_t ws_fwd, ws_bwd, ws_fwd_bytes, ws_bwd_bytes;
   size_t total;
@@ -95,12 +96,13 @@ HostPassLayout host_pass_layout(const loong_attn_desc& d, int pass) {
   const size_t out_shape[4] = {L.q, L.q, L.kv, L.kv};  // o, dq, dk, dv
   for (int t = 0; t < 4; ++t) L.out[t] = (t > 0 && pass == 0) ? 0 : take(out_shape[t]);
   L.lse_off = take(L.lse);
+  L.ores = pass == 1 ? take(L.q) : 0;
   if (d.layout == LOONG_LAYOUT_RANK_MAJOR) {
     const size_t kt_shape[8] = {L.q, L.kv, L.kv, L.q, L.q, L.q, L.kv, L.kv};
     for (int t = 0; t < 8; ++t) L.kt[t] = ((t == 3 || t > 4) && pass == 0) ? 0 : take(kt_shape[t]);
   }
   L.ws_fwd_bytes = loong_attn_workspace_size(&d, 0);
-  L.ws_fwd = L.ws_fwd_bytes ? take(L.ws_fwd_bytes) : 0;
+  L.ws_fwd = take(L.ws_fwd_bytes);
   L.ws_bwd_bytes = pass == 1 ? loong_attn_workspace_size(&d, 1) : 0;
   L.ws_bwd = L.ws_bwd_bytes ? take(L.ws_bwd_bytes) : 0;
   L.total = off;
@@ -191,13 +193,15 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
   if (pass == 0 && rm) LOONG_TRY(cudaEventRecord(hp->slot_free[slot], stream));
   LOONG_TRY(cudaStreamWaitEvent(stream, hp->o_lse_out, 0));
   float* lse_dev = static_cast<float*>(at(L.lse_off));
-  void* ws_fwd = L.ws_fwd_bytes ? at(L.ws_fwd) : nullptr;
+  void* ws_fwd = at(L.ws_fwd);
+  // the residual of O stays on the device for the backward's D
+  void* o_res = pass == 1 ? at(L.ores) : nullptr;
   if (rm) {
-    if ((st = loong_attn_fwd(d, at(L.kt[0]), at(L.kt[1]), at(L.kt[2]), at(L.kt[4]), lse_dev, ws_fwd, L.ws_fwd_bytes,
-                             stream_)) != LOONG_OK)
+    if ((st = loong_attn_fwd(d, at(L.kt[0]), at(L.kt[1]), at(L.kt[2]), at(L.kt[4]), lse_dev, o_res, ws_fwd,
+                             L.ws_fwd_bytes, stream_)) != LOONG_OK)
       return st;
     if ((st = repack(4, 1, L.out, 1)) != LOONG_OK) return st;
-  } else if ((st = loong_attn_fwd(d, at(in[0]), at(in[1]), at(in[2]), at(L.out[0]), lse_dev, ws_fwd,
+  } else if ((st = loong_attn_fwd(d, at(in[0]), at(in[1]), at(in[2]), at(L.out[0]), lse_dev, o_res, ws_fwd,
                                   L.ws_fwd_bytes, stream_)) != LOONG_OK) {
     return st;
   }
@@ -216,14 +220,14 @@ int loong_attn_2d_host(const loong_attn_desc* d, int32_t slot, const void* q, co
     if (rm) {
       if ((st = repack(3, 1, in + 3, 0)) != LOONG_OK) return st;
       LOONG_TRY(cudaEventRecord(hp->slot_free[slot], stream));
-      if ((st = loong_attn_bwd(d, at(L.kt[0]), at(L.kt[1]), at(L.kt[2]), at(L.kt[4]), lse_dev, at(L.kt[3]),
+      if ((st = loong_attn_bwd(d, at(L.kt[0]), at(L.kt[1]), at(L.kt[2]), at(L.kt[4]), o_res, lse_dev, at(L.kt[3]),
                                at(L.kt[5]), at(L.kt[6]), at(L.kt[7]), ws_bwd, L.ws_bwd_bytes, stream_)) != LOONG_OK)
         return st;
       LOONG_TRY(cudaStreamWaitEvent(stream, hp->grads_out, 0));
       if ((st = repack(5, 3, L.out + 1, 1)) != LOONG_OK) return st;
     } else {
       LOONG_TRY(cudaStreamWaitEvent(stream, hp->grads_out, 0));
-      if ((st = loong_attn_bwd(d, at(in[0]), at(in[1]), at(in[2]), at(L.out[0]), lse_dev, at(in[3]),
+      if ((st = loong_attn_bwd(d, at(in[0]), at(in[1]), at(in[2]), at(L.out[0]), o_res, lse_dev, at(in[3]),
                                at(L.out[1]), at(L.out[2]), at(L.out[3]), ws_bwd, L.ws_bwd_bytes, stream_)) != LOONG_OK)
         return st;
       LOONG_TRY(cudaEventRecord(hp->slot_free[slot], stream));

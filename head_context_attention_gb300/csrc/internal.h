@@ -73,21 +73,39 @@ inline bool is_copy_mode(const loong_attn_desc& d) {
 // Token/head placement of the descriptor's tensors (natural or rank-major).
 Layout layout_of(const loong_attn_desc& d);
 
+// The forward's workspace and optional outputs.
+struct FwdScratch {
+  void* v16 = nullptr;          // fp16 V * 2^-e, the layout of V
+  unsigned* v_amax = nullptr;   // bit pattern of max |V| (v16_shift gives e)
+  float* o_acc = nullptr;       // STEPWISE: fp32 O accumulator
+  void* kv_recv = nullptr;      // STEPWISE_COPY: K0, K1, V0, V1 receive buffers (exchange.h)
+  void* o_res = nullptr;        // bf16 rounding residual of O, or null
+};
+// Byte offsets of the forward workspace's parts (each on a 256-byte boundary)
+// and its total size.
+struct FwdWsLayout {
+  size_t v16, amax, o_acc, recv, total;
+};
+FwdWsLayout fwd_ws_layout(const loong_attn_desc& d);
+
 // Kernel launchers (asynchronous on `stream`).
 // Query rows of ring ranks [rank_begin, rank_end) only (all of them: 0, cp).
-// STEPWISE_COPY: kv_recv holds the K0, K1, V0, V1 receive buffers (exchange.h).
+// The forward first writes V's fp16 copy into sc.v16.
 int launch_fwd(const loong_attn_desc& d, const void* q, const void* k, const void* v, void* o,
-               float* lse, float* o_acc, cudaStream_t stream, int rank_begin = 0, int rank_end = -1,
-               void* kv_recv = nullptr);
+               float* lse, const FwdScratch& sc, cudaStream_t stream, int rank_begin = 0, int rank_end = -1);
+// o_res: the forward's residual of O, or null (D from O alone).
 int launch_bwd(const loong_attn_desc& d, const void* q, const void* k, const void* v,
-               const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+               const void* o, const void* o_res, const float* lse, const void* dout, void* dq, void* dk, void* dv,
                float* dq_acc, float* dvec, float* dk_acc, float* dv_acc, cudaStream_t stream,
                void* kv_recv = nullptr);
+// max |V| into *amax (two launches: the maximum, then V * 2^-e as fp16 into v16).
+int launch_v_to_f16(const void* v, void* v16, unsigned* amax, int64_t n, cudaStream_t stream);
 
 int launch_fill_f32(float* p, int64_t n, float value, cudaStream_t stream);
 // One CTA whose bounded mbarrier wait has nothing to wait for (selftest.cu).
 int launch_wait_probe(uint32_t limit_us, cudaStream_t stream);
-int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream);
+// out = bf16(in); with res, also res = bf16(in - out) (the rounding residual).
+int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream, void* res = nullptr);
 int launch_lse_merge(int64_t rows, int d, int n_parts, const float* o_parts,
                      const float* lse_parts, void* o_out, float* lse_out, int out_bf16,
                      cudaStream_t stream);
@@ -103,7 +121,8 @@ inline int stat_block_pad(int blk) { return (blk + 3) & ~3; }
 inline int64_t stat_row_len(const RingGeom& g) {
   return static_cast<int64_t>(g.nblocks) * stat_block_pad(g.blk) + kTile;
 }
-int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* dout, const float* lse,
-                        float* stats, cudaStream_t stream);
+// With o_res, D = rowsum(dO * (O + O_res)).
+int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* o_res, const void* dout,
+                        const float* lse, float* stats, cudaStream_t stream);
 
 }  // namespace loong

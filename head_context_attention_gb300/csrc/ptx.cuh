@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -287,30 +288,30 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16: fp16 A and B (format code 0), fp32
+// accumulator.  A and B of one MMA always share their type.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) | (static_cast<uint32_t>(b_mn_major) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The forward's P V product takes fp16 operands (11 significant bits against
+// bf16's 8, so the probabilities lose less).  V is stored as V * 2^-e with e
+// chosen from the bit pattern of max |V| (a non-negative float) so that the
+// largest |V * 2^-e| lies in [2^14, 2^15): inside fp16's range and clear of
+// its subnormals whatever V's scale.  The forward multiplies O by 2^e at the
+// end (exact).  e is clamped to [-100, 114] so that 2^e and 2^-e stay normal
+// floats (only an all-zero, subnormal or non-finite V reaches the clamp).
+__host__ __device__ constexpr int v16_shift(uint32_t amax_bits) {
+  const int e = static_cast<int>((amax_bits >> 23) & 0xFFu) - 127 - 14;  // floor(log2 max|V|) - 14
+  return e < -100 ? -100 : (e > 114 ? 114 : e);
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x on the FMA pipe, for offloading part of the softmax exponentials from
-// the MUFU unit.  Cody-Waite style reduction: n = round(x) (the 1.5*2^23 shift
-// leaves n in the low mantissa bits), f = x - n in [-1/2, 1/2], 2^f from a
-// degree-3 polynomial with constant term 1 whose coefficients are a discrete
-// minimax fit of the relative error (fit_exp2_poly.py), and 2^n added into the
-// exponent field.  Relative error <= 1.1e-4 for x in [-126, 8], below the
-// 2^-9 rounding of the bf16 probabilities it feeds.  x <= -127 (including
-// -inf) returns +0.
-__device__ __forceinline__ float exp2_fma(float x) {
-  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
-  constexpr float c1 = 6.932829022e-01f, c2 = 2.422109693e-01f, c3 = 5.500905961e-02f;
-  x = fmaxf(x, -127.0f);
-  const float t = x + kShift;
-  const float f = x - (t - kShift);
-  const float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, 1.0f);
-  const int n = __float_as_int(t) - __float_as_int(kShift);
-  return __int_as_float(__float_as_int(p) + (n << 23));
 }
 
 // max(a, b, c) in one instruction (sm_100 family); exact, like fmaxf twice.
@@ -322,6 +323,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -45,9 +45,15 @@ __global__ void fill_f32_kernel(float* p, int64_t n, float value) {
     p[i] = value;
 }
 
-// n % 8 == 0 handled by the vector path; the tail element by element.
+__device__ __forceinline__ float bf16_residual(float x) {
+  return x - __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// n % 8 == 0 handled by the vector path; the tail element by element.  With
+// res, also the rounding residual bf16(x - bf16(x)) (exact before its own
+// rounding).
 __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* __restrict__ out,
-                                   int64_t n) {
+                                   __nv_bfloat16* __restrict__ res, int64_t n) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t nv = n / 8;
   const float4* in4 = reinterpret_cast<const float4*>(in);
@@ -60,10 +66,53 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, __nv_bfloat16* 
     w.z = pack_bf16(b.x, b.y);
     w.w = pack_bf16(b.z, b.w);
     out4[i] = w;
+    if (res) {
+      uint4 r;
+      r.x = pack_bf16(bf16_residual(a.x), bf16_residual(a.y));
+      r.y = pack_bf16(bf16_residual(a.z), bf16_residual(a.w));
+      r.z = pack_bf16(bf16_residual(b.x), bf16_residual(b.y));
+      r.w = pack_bf16(bf16_residual(b.z), bf16_residual(b.w));
+      reinterpret_cast<uint4*>(res)[i] = r;
+    }
   }
   for (int64_t i = nv * 8 + blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += stride)
+       i += stride) {
     out[i] = __float2bfloat16_rn(in[i]);
+    if (res) res[i] = __float2bfloat16_rn(bf16_residual(in[i]));
+  }
+}
+
+// max |x| over the n bf16 values of `in` (n % 8 == 0), as the bit pattern of
+// a non-negative float, atomically maxed into *amax (zeroed by the caller).
+// With the sign cleared, bf16 bit patterns order like the values they encode.
+__global__ void absmax_bf16_kernel(const uint4* __restrict__ in, int64_t nvec, unsigned* amax) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  unsigned m = 0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nvec; i += stride) {
+    const uint4 x = __ldg(in + i);
+    const unsigned w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m = max(m, max(w[u] & 0x7FFFu, (w[u] >> 16) & 0x7FFFu));
+  }
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m) atomicMax(amax, m << 16);
+}
+
+// out = fp16(in * 2^-e), e = v16_shift(*amax): the largest value lands in
+// [2^14, 2^15).
+__global__ void bf16_to_f16_scaled_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, int64_t nvec,
+                                          const unsigned* __restrict__ amax) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const float f = __int_as_float((127 - v16_shift(*amax)) << 23);  // 2^-e, -100 <= e <= 114
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nvec; i += stride) {
+    const uint4 x = __ldg(in + i);
+    const unsigned w[4] = {x.x, x.y, x.z, x.w};
+    unsigned y[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      y[u] = pack_f16(__uint_as_float(w[u] << 16) * f, __uint_as_float(w[u] & 0xFFFF0000u) * f);
+    out[i] = make_uint4(y[0], y[1], y[2], y[3]);
+  }
 }
 
 // Unsigned division by a divisor fixed for the launch, n < 2^31: the
@@ -353,10 +402,12 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
 // Backward row statistics (see stat_row_len): for row (b, s, h) of O and dO
 // (rows enumerated in natural order, read where `lay` keeps them),
 // D = sum_d dO*O in fp32 and LSE*log2(e), written at the padded position of
-// token s.  16 threads per row of 128 bf16 (8 elements each), 8 for d = 64.
+// token s.  With o_res, O is taken as O + O_res (exact in fp32: the residual
+// holds the next 8 bits).  16 threads per row of 128 bf16 (8 elements each),
+// 8 for d = 64.
 template <int D>
-__global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                                    const float* __restrict__ lse, float* __restrict__ lse2,
+__global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_res,
+                                    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, float* __restrict__ lse2,
                                     float* __restrict__ dstat, int64_t rows, int64_t S, int hq, int blk,
                                     int blk_pad, int64_t stat_len, Layout lay, unsigned* err) {
   constexpr int TPR = D / 8;
@@ -381,14 +432,17 @@ __global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const _
     if (live && row_ok) {
       const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + off) + part);
       const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + off) + part);
+      const uint4 rv = o_res ? __ldg(reinterpret_cast<const uint4*>(o_res + off) + part) : make_uint4(0, 0, 0, 0);
       const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
       const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 fa = __bfloat1622float2(a2[e]);
+        const float2 fr = __bfloat1622float2(r2[e]);
         const float2 fb = __bfloat1622float2(b2[e]);
-        acc = fmaf(fa.x, fb.x, acc);
-        acc = fmaf(fa.y, fb.y, acc);
+        acc = fmaf(fa.x + fr.x, fb.x, acc);
+        acc = fmaf(fa.y + fr.y, fb.y, acc);
       }
     }
 #pragma unroll
@@ -412,9 +466,23 @@ int launch_fill_f32(float* p, int64_t n, float value, cudaStream_t stream) {
   return check_launch();
 }
 
-int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream) {
+int launch_f32_to_bf16(const float* in, void* out, int64_t n, cudaStream_t stream, void* res) {
   if (n <= 0) return LOONG_OK;
-  f32_to_bf16_kernel<<<grid_for(n / 8 + 1, 256, 8), 256, 0, stream>>>(in, static_cast<__nv_bfloat16*>(out), n);
+  f32_to_bf16_kernel<<<grid_for(n / 8 + 1, 256, 8), 256, 0, stream>>>(in, static_cast<__nv_bfloat16*>(out),
+                                                                      static_cast<__nv_bfloat16*>(res), n);
+  return check_launch();
+}
+
+int launch_v_to_f16(const void* v, void* v16, unsigned* amax, int64_t n, cudaStream_t stream) {
+  if (n <= 0 || n % 8) return LOONG_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int64_t nvec = n / 8;
+  absmax_bf16_kernel<<<grid_for(nvec, 256, 8), 256, 0, stream>>>(static_cast<const uint4*>(v), nvec, amax);
+  int st = check_launch();
+  if (st != LOONG_OK) return st;
+  bf16_to_f16_scaled_kernel<<<grid_for(nvec, 256, 8), 256, 0, stream>>>(static_cast<const uint4*>(v),
+                                                                        static_cast<uint4*>(v16), nvec, amax);
   return check_launch();
 }
 
@@ -501,24 +569,25 @@ int launch_headctx_pack(int n, int64_t batch, int cp, int P, int64_t s_local, co
   return check_launch();
 }
 
-int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* dout, const float* lse,
-                        float* stats, cudaStream_t stream) {
+int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* o_res, const void* dout,
+                        const float* lse, float* stats, cudaStream_t stream) {
   const RingGeom g = ring_geom(d);
   const int64_t rows = d.batch * d.seqlen * d.hq;
   const int64_t stat_len = stat_row_len(g);
   float* lse2 = stats;
   float* dstat = stats + d.batch * d.hq * stat_len;
   const auto* po = static_cast<const __nv_bfloat16*>(o);
+  const auto* pr = static_cast<const __nv_bfloat16*>(o_res);
   const auto* pd = static_cast<const __nv_bfloat16*>(dout);
   const int bp = stat_block_pad(g.blk);
   unsigned* err = device_error_word();
   if (!err) return LOONG_ERR_CUDA;
   if (d.head_dim == 128)
     bwd_rowstats_kernel<128><<<grid_for(rows * 16, 256, 8), 256, 0, stream>>>(
-        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
+        po, pr, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
   else if (d.head_dim == 64)
     bwd_rowstats_kernel<64><<<grid_for(rows * 8, 256, 8), 256, 0, stream>>>(
-        po, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
+        po, pr, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
   else
     return LOONG_ERR_UNSUPPORTED;
   return check_launch();

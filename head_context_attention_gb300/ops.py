@@ -76,10 +76,10 @@ def lib():
         L.loong_attn_workspace_size.restype = SZ
         L.loong_attn_workspace_size.argtypes = [D, ctypes.c_int]
         L.loong_ring_schedule.argtypes = [I32, I32, ctypes.POINTER(ctypes.c_int32)]
-        L.loong_attn_fwd.argtypes = [D, P, P, P, P, P, P, SZ, P]
-        L.loong_attn_fwd_ranks.argtypes = [D, I32, I32, P, P, P, P, P, P]
-        L.loong_attn_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, SZ, P]
-        L.loong_attn_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P]
+        L.loong_attn_fwd.argtypes = [D, P, P, P, P, P, P, P, SZ, P]
+        L.loong_attn_fwd_ranks.argtypes = [D, I32, I32, P, P, P, P, P, P, SZ, P]
+        L.loong_attn_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+        L.loong_attn_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P]
         L.loong_lse_merge.argtypes = [I64, I32, I32, P, P, P, P, ctypes.c_int, P]
         L.loong_headctx_pack.argtypes = [I64, I32, I32, I64, I32, I32, ctypes.c_int, ctypes.c_int,
                                          P, P, P]
@@ -133,24 +133,32 @@ def loong_ring_schedule(inner, outer):
     return [[buf[t * cp + c] for c in range(cp)] for t in range(cp)]
 
 
-def loong_attn_fwd(desc, q, k, v, o, lse, ws=None, stream=None):
-    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+def _nbytes(ws):
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+def loong_attn_fwd(desc, q, k, v, o, lse, o_res, ws, stream=None):
     return _check("loong_attn_fwd", lib().loong_attn_fwd(
-        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws), nbytes,
-        _stream(stream)))
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(o_res), _ptr(ws),
+        _nbytes(ws), _stream(stream)))
 
 
-def loong_attn_fwd_ranks(desc, rank_begin, rank_end, q, k, v, o, lse, stream=None):
+def loong_attn_fwd_ranks(desc, rank_begin, rank_end, q, k, v, o, lse, ws, stream=None):
     return _check("loong_attn_fwd_ranks", lib().loong_attn_fwd_ranks(
         ctypes.byref(desc), rank_begin, rank_end, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-        _stream(stream)))
+        _ptr(ws), _nbytes(ws), _stream(stream)))
 
 
-def loong_attn_bwd(desc, q, k, v, o, lse, dout, dq, dk, dv, ws, stream=None):
-    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+def loong_attn_bwd(desc, q, k, v, o, o_res, lse, dout, dq, dk, dv, ws, stream=None):
     return _check("loong_attn_bwd", lib().loong_attn_bwd(
-        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
-        _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream(stream)))
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(dout),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _nbytes(ws), _stream(stream)))
+
+
+def loong_attn_bwd_noalloc(desc, q, k, v, o, o_res, lse, dout, dq, dk, dv, stream=None):
+    return _check("loong_attn_bwd_noalloc", lib().loong_attn_bwd_noalloc(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_res), _ptr(lse), _ptr(dout),
+        _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
 
 def loong_lse_merge(o_parts, lse_parts, o_out, lse_out, stream=None):
@@ -215,23 +223,27 @@ def workspace(desc, pass_, device="cuda"):
     return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def attn_fwd(w, q, k, v, mode=MODE_FUSED, stream=None, layout=LAYOUT_NATURAL):
-    """Allocate O and LSE with torch, run loong_attn_fwd, return (o, lse).
-    With LAYOUT_RANK_MAJOR, q/k/v (and o) are headctx_pack outputs."""
+def attn_fwd(w, q, k, v, mode=MODE_FUSED, stream=None, layout=LAYOUT_NATURAL, res=True):
+    """Allocate O, LSE (and O's rounding residual) with torch, run
+    loong_attn_fwd, return (o, lse, o_res); o_res is None when ``res`` is
+    false.  With LAYOUT_RANK_MAJOR, q/k/v (and o) are headctx_pack outputs."""
     desc = make_desc(w, mode, layout=layout)
     _check("loong_attn_check", loong_attn_check(desc))
     o = torch.empty_like(q)
+    o_res = torch.empty_like(q) if res else None
     lse = torch.empty((w.batch, w.hq, w.seqlen), dtype=torch.float32, device=q.device)
-    loong_attn_fwd(desc, q, k, v, o, lse, workspace(desc, 0, q.device), stream)
-    return o, lse
+    loong_attn_fwd(desc, q, k, v, o, lse, o_res, workspace(desc, 0, q.device), stream)
+    return o, lse, o_res
 
 
-def attn_bwd(w, q, k, v, o, lse, do, mode=MODE_FUSED, stream=None, layout=LAYOUT_NATURAL):
-    """Allocate dQ/dK/dV with torch, run loong_attn_bwd, return them (in the layout of q, k)."""
+def attn_bwd(w, q, k, v, o, lse, do, o_res=None, mode=MODE_FUSED, stream=None, layout=LAYOUT_NATURAL):
+    """Allocate dQ/dK/dV with torch, run loong_attn_bwd, return them (in the
+    layout of q, k).  ``o_res``: the forward's residual of O (D from O + o_res),
+    or None (D from O alone)."""
     desc = make_desc(w, mode, layout=layout)
     _check("loong_attn_check", loong_attn_check(desc))
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    loong_attn_bwd(desc, q, k, v, o, lse, do, dq, dk, dv, workspace(desc, 1, q.device), stream)
+    loong_attn_bwd(desc, q, k, v, o, o_res, lse, do, dq, dk, dv, workspace(desc, 1, q.device), stream)
     return dq, dk, dv
 
 

@@ -11,8 +11,8 @@
  *       Head-Context Parallelism" (abstract page)
  *
  * Conventions shared by every entry point
- *   - Pointers named q, k, v, o, dout, dq, dk, dv, lse, ws, in, out, o_parts,
- *     lse_parts, o_out, lse_out are DEVICE pointers owned by the caller:
+ *   - Pointers named q, k, v, o, o_res, dout, dq, dk, dv, lse, ws, in, out,
+ *     o_parts, lse_parts, o_out, lse_out are DEVICE pointers owned by the caller:
  *     memory of the current device, from cudaMalloc or managed.  A host
  *     pointer (pinned or not) or another device's memory is refused with
  *     LOONG_ERR_INVALID_ARG before any work is enqueued.  The
@@ -151,8 +151,10 @@ LOONG_API int loong_attn_check(const loong_attn_desc* desc);
 /*
  * Device workspace, in bytes, that loong_attn_fwd (pass 0) or loong_attn_bwd
  * (pass 1) needs for `desc`; 0 for an invalid descriptor.  Host-only.
- *   fwd, FUSED: 0.  fwd, STEPWISE: fp32 O accumulator, B*S*Hq*d values.
- *   STEPWISE_COPY adds, to both passes, four bf16 receive buffers of
+ *   fwd: the fp16 copy of V that the P V product reads (B*S*Hkv*d values of
+ *        2 bytes) and one word for max |V|; STEPWISE adds the fp32 O
+ *        accumulator, B*S*Hq*d values.
+ *   STEPWISE_COPY adds, to both passes, four 2-byte receive buffers of
  *        B*S*Hkv*d values each (K and V, two of each).
  *   bwd: fp32 dQ accumulator (B*S*Hq*d) + fp32 row statistics (LSE*log2 e
  *        and D = rowsum(dO*O)), 2 x B x Hq x (nblocks*roundup(blk,4) + 128)
@@ -176,15 +178,22 @@ LOONG_API int loong_ring_schedule(int32_t ring_inner, int32_t ring_outer, int32_
  * computes causal softmax attention of rank c's query blocks against the K/V
  * blocks of rank src(c, t) and merges the step's result into the running
  * result by log-sum-exp.  The result equals causal attention over the whole
- * sequence up to rounding.
+ * sequence up to rounding.  The probabilities enter the P V product as fp16
+ * (V as a scaled fp16 copy in the workspace) and accumulation is fp32, so the
+ * unrounded O is within about 2^-12 of exact attention.
  *   q, k, v   inputs (layouts above), read only.
  *   o         bf16 output, the layout of q.
  *   lse       fp32 output [B,Hq,S].
+ *   o_res     NULL, or a bf16 output in the layout of q: the rounding
+ *             residual of O, bf16(O32 - bf16(O32)) with O32 the fp32 result,
+ *             so that O + o_res holds O32 to about 16 bits.  Pass it to
+ *             loong_attn_bwd, which then forms D = rowsum(dO * O) from
+ *             O + o_res.
  *   ws        device workspace of at least loong_attn_workspace_size(desc,0)
- *             bytes (may be NULL when that size is 0).
+ *             bytes; every descriptor needs one.
  */
 LOONG_API int loong_attn_fwd(const loong_attn_desc* desc, const void* q, const void* k, const void* v,
-                   void* o, float* lse, void* ws, size_t ws_bytes, loong_stream_t stream);
+                   void* o, float* lse, void* o_res, void* ws, size_t ws_bytes, loong_stream_t stream);
 
 /*
  * loong_attn_fwd restricted to the query rows of ring ranks
@@ -193,11 +202,12 @@ LOONG_API int loong_attn_fwd(const loong_attn_desc* desc, const void* q, const v
  * timed ([G] section 2 gives every rank the same work under paired blocks).
  * Rows of other ranks in o and lse are left untouched; the rows written equal
  * those of loong_attn_fwd bit for bit.  FUSED mode only (STEPWISE returns
- * LOONG_ERR_UNSUPPORTED); no workspace.  0 <= rank_begin < rank_end <= cp.
+ * LOONG_ERR_UNSUPPORTED); ws as for loong_attn_fwd.  0 <= rank_begin <
+ * rank_end <= cp.
  */
 LOONG_API int loong_attn_fwd_ranks(const loong_attn_desc* desc, int32_t rank_begin, int32_t rank_end,
                                    const void* q, const void* k, const void* v, void* o, float* lse,
-                                   loong_stream_t stream);
+                                   void* ws, size_t ws_bytes, loong_stream_t stream);
 
 /*
  * Backward of loong_attn_fwd: the exact gradient of causal softmax attention
@@ -206,19 +216,29 @@ LOONG_API int loong_attn_fwd_ranks(const loong_attn_desc* desc, int32_t rank_beg
  * dS = P * (dP - D) with D = rowsum(dO * O), dQ += scale dS K,
  * dK += scale dS^T Q; dK and dV sum over the query heads of a kv group.
  *   o, lse    the outputs of loong_attn_fwd for the same inputs.
+ *   o_res     the forward's o_res output, or NULL.  D is formed in fp32 from
+ *             O + o_res, else from the bf16 O alone.  The D term of dQ and dK
+ *             is -scale * D * (probability-weighted keys or queries), so an
+ *             error in D is amplified where a few large keys take the
+ *             probability mass; with o_res, D carries the forward's own
+ *             accuracy instead of bf16's 2^-9.
  *   dout      bf16 dO, the layout of q.
  *   dq        bf16, the layout of q; dk, dv bf16, the layout of k; written,
  *             not added to.
  *   ws        at least loong_attn_workspace_size(desc,1) bytes.
  */
 LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const void* k, const void* v,
-                   const void* o, const float* lse, const void* dout,
+                   const void* o, const void* o_res, const float* lse, const void* dout,
                    void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
                    loong_stream_t stream);
 
 /*
- * Largest workspace, in bytes, that loong_attn_bwd_noalloc can serve: 32 MiB,
- * e.g. S = 8192 tokens x 8 query heads x d = 128 in FUSED mode.
+ * Largest workspace, in bytes, that loong_attn_bwd_noalloc can serve: 32 MiB.
+ * A problem fits when loong_attn_workspace_size(desc, 1) is at most this; in
+ * FUSED mode that size is at most 4*B*S*Hq*d + 8*B*S*Hkv*d +
+ * 8*B*Hq*(S + 3*nblocks + 128) bytes plus 256 per part (four parts), with
+ * nblocks = 2cp (ZIGZAG) or cp.  For example S = 4096 tokens, Hq = 8, Hkv = 1,
+ * d = 128 needs about 20.3 MiB.
  */
 #define LOONG_NOALLOC_SCRATCH_BYTES (32u << 20)
 
@@ -229,6 +249,9 @@ LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const v
  * that cannot take cudaMalloc's implicit device synchronisation.  The paper
  * has no counterpart; this is an interface convenience.
  *   Same arguments, layouts and results as loong_attn_bwd, minus ws/ws_bytes.
+ *   The descriptor is checked first, then the device (LOONG_ERR_UNSUPPORTED
+ *   on one that is not compute capability 10.3); a problem whose workspace
+ *   exceeds the array gives LOONG_ERR_WORKSPACE.
  *   Scratch lives in one static device array of LOONG_NOALLOC_SCRATCH_BYTES
  *   that every GPU loading the library holds until the process exits.  The
  *   call allocates nothing: no cudaMalloc, cudaFree or allocating library
@@ -236,15 +259,16 @@ LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const v
  *   loong_attn_workspace_size(desc, 1) exceeds LOONG_NOALLOC_SCRATCH_BYTES.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  A failed lookup is not remembered: the next
+ *   call tries again.
  *   Every call on a device shares the one array and it keeps the last call's
  *   contents (the parts that must start at zero are cleared by each call):
  *   calls whose work overlaps on the GPU (other streams, other host threads)
  *   race on it and must be serialised by the caller.
  */
 LOONG_API int loong_attn_bwd_noalloc(const loong_attn_desc* desc, const void* q, const void* k,
-                                     const void* v, const void* o, const float* lse, const void* dout,
-                                     void* dq, void* dk, void* dv, loong_stream_t stream);
+                                     const void* v, const void* o, const void* o_res, const float* lse,
+                                     const void* dout, void* dq, void* dk, void* dv, loong_stream_t stream);
 
 /*
  * n-way log-sum-exp merge of partial attention results over disjoint key sets
@@ -299,7 +323,8 @@ LOONG_API int loong_headctx_pack_n(int32_t n, int64_t batch, int32_t cp, int32_t
  * Device workspace, in bytes, of loong_attn_2d_host for `desc`: pass 0 runs
  * the forward alone, pass 1 the forward and the backward; 0 for an invalid
  * descriptor.  Host-only.  It holds two sets of natural-layout inputs (the
- * slots), the natural-layout outputs and LSE, the rank-major tensors of the
+ * slots), the natural-layout outputs and LSE, the forward's residual of O
+ * (pass 1: the backward forms D from O and it), the rank-major tensors of the
  * pass (RANK_MAJOR) and the workspaces of loong_attn_fwd / loong_attn_bwd,
  * each part on a 256-byte boundary.
  */

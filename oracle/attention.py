@@ -17,8 +17,9 @@ Readings where the pages are silent:
     D_i = dO_i . O_i, dP = dO V^T, dS = P * (dP - D), dQ = scale dS K,
     dK = scale dS^T Q, dV = P^T dO, with dK and dV summed over the query heads
     that share a kv head.  Optionally (``d_from_bf16_o``) D is formed from O
-    rounded to bf16, the output the forward returns; with peaky logits this
-    rounding moves dQ by up to ~0.1 (keys scaled x8 at S = 1M).
+    rounded to bf16: the reading for a backward that is given only the bf16
+    output of the forward (with peaky logits this moves dQ by up to ~0.1 at
+    keys scaled x8 and S = 1M).
 
 Layouts: q [S, Hq, d], k and v [S, Hkv, d], o [S, Hq, d], lse [Hq, S].  The
 batch dimension is handled by the caller (B = 1 in every workload).
@@ -159,8 +160,7 @@ def attention_rows(q, k, v, rows, heads, scale=None):
     return o, lse
 
 
-def attention_backward_rows(q, k, v, do, rows, heads, scale=None, d_from_bf16_o=False,
-                            with_d_bound=False):
+def attention_backward_rows(q, k, v, do, rows, heads, scale=None, d_from_bf16_o=False):
     """dQ for selected query rows of selected heads (causal).
 
     dQ_i = scale * sum_{j<=i} P_ij (dP_ij - D_i) k_j with D_i = dO_i . O_i,
@@ -175,7 +175,6 @@ def attention_backward_rows(q, k, v, do, rows, heads, scale=None, d_from_bf16_o=
     rows = np.asarray(rows, dtype=np.int64)
     o, lse = attention_rows(q, k, v, rows, heads, scale)
     dq = np.zeros((len(heads), len(rows), d))
-    bound = np.zeros_like(dq)
     group = max(1, int(2 ** 25 // max(1, k.shape[0])))
     for a, h in enumerate(heads):
         kh = np.ascontiguousarray(k[:, h // g, :])
@@ -190,14 +189,10 @@ def attention_backward_rows(q, k, v, do, rows, heads, scale=None, d_from_bf16_o=
             dp = do[rr, h, :] @ vh[:n].T
             ds = p * (dp - dvec[:, None])
             dq[a, r0:r0 + group] = scale * (ds @ kh[:n])
-            if with_d_bound:
-                bound[a, r0:r0 + group] = d_rounding_bounds(p, vh[:n], o[a, r0:r0 + group], do[rr, h, :],
-                                                            kh[:n], scale, "rows")
-    return (dq, bound) if with_d_bound else dq
+    return dq
 
 
-def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None, d_from_bf16_o=False,
-                            with_d_bound=False):
+def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None, d_from_bf16_o=False):
     """dK and dV for selected key positions of one kv head (causal).
 
     dV_j = sum_{h in group} sum_{i>=j} P_ij dO_i and
@@ -219,7 +214,6 @@ def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None, d_from_bf16_
     vj = v[keys, kv_head, :]
     dk = np.zeros((len(keys), d))
     dv = np.zeros((len(keys), d))
-    bound = np.zeros_like(dk)
     for a, h in enumerate(heads):
         qh = q[rows, h, :]
         doh = do[rows, h, :]
@@ -231,39 +225,4 @@ def attention_backward_keys(q, k, v, do, keys, kv_head, scale=None, d_from_bf16_
         ds = p * (dp - dvec[:, None])
         dv += p.T @ doh
         dk += scale * (ds.T @ qh)
-        if with_d_bound:
-            # the full rows' P is needed for sum_j P_ij |V_j|: recompute it over all keys <= i
-            vh = v[:, kv_head, :]
-            kh = k[:, kv_head, :]
-            for r0 in range(0, len(rows), 256):
-                rr = rows[r0:r0 + 256]
-                n = int(rr.max()) + 1
-                sf = scale * (qh[r0:r0 + 256] @ kh[:n].T)
-                sf = np.where(np.arange(n)[None, :] > rr[:, None], -np.inf, sf)
-                pf = np.exp(sf - lse[a][r0:r0 + 256][:, None])
-                dd = BF16_UNIT_ROUNDOFF * np.sum(np.abs(doh[r0:r0 + 256]) *
-                                                 (pf @ np.abs(vh[:n]) + np.abs(o[a][r0:r0 + 256])), axis=1)
-                bound += scale * (p[r0:r0 + 256].T * dd[None, :]) @ np.abs(qh[r0:r0 + 256])
-    return (dk, dv, bound) if with_d_bound else (dk, dv)
-
-
-BF16_UNIT_ROUNDOFF = 2.0 ** -8
-
-
-def d_rounding_bounds(p, v, o, do, k_or_q, scale, axis):
-    """First-order bound on the change of the D term of dQ (or dK).
-
-    A CUDA forward forms O from bf16-rounded probabilities and returns O rounded
-    to bf16; D = dO . O then carries |dD_i| <= u * sum_d |dO_id| *
-    (sum_j P_ij |V_jd| + |O_id|), u = 2^-8 the bf16 unit roundoff.  The D term
-    of dQ_i is -scale * D_i * sum_j P_ij k_j, so it moves by at most
-    scale * |dD_i| * |sum_j P_ij k_jd|; for dK_j it is -scale * sum_i P_ij D_i
-    q_i, moving by at most scale * sum_i P_ij |dD_i| |q_id|.
-
-    p [rows, keys], v [keys, d], o / do [rows, d]; ``k_or_q`` is k [keys, d]
-    (axis="rows": bound for dQ rows) or q [rows, d] (axis="keys": dK keys).
-    """
-    dd = BF16_UNIT_ROUNDOFF * np.sum(np.abs(do) * (p @ np.abs(v) + np.abs(o)), axis=1)
-    if axis == "rows":
-        return scale * dd[:, None] * np.abs(p @ k_or_q)
-    return scale * (p.T * dd[None, :]) @ np.abs(k_or_q)
+    return dk, dv

@@ -86,11 +86,14 @@ def test_workspace_sizes(loong_lib):
     fused, step = ops.make_desc(w, ops.MODE_FUSED), ops.make_desc(w, ops.MODE_STEPWISE)
     q_el = w.seqlen * w.hq * w.head_dim
     kv_el = w.seqlen * w.hkv * w.head_dim
-    assert ops.loong_attn_workspace_size(fused, 0) == 0
-    assert ops.loong_attn_workspace_size(step, 0) == q_el * 4
+    up = lambda x: (x + 255) // 256 * 256
+    # the forward's fp16 copy of V and the word for max |V|; STEPWISE adds the fp32 O accumulator
+    assert ops.loong_attn_workspace_size(fused, 0) == up(kv_el * 2) + 256
+    assert ops.loong_attn_workspace_size(step, 0) == up(kv_el * 2) + 256 + q_el * 4
+    copy = ops.make_desc(w, ops.MODE_STEPWISE_COPY, layout=ops.LAYOUT_RANK_MAJOR)
+    assert ops.loong_attn_workspace_size(copy, 0) == up(kv_el * 2) + 256 + q_el * 4 + 4 * up(kv_el * 2)
     blk = w.seqlen // (2 * w.cp)
     stats = 2 * w.hq * (2 * w.cp * ((blk + 3) // 4 * 4) + 128) * 4
-    up = lambda x: (x + 255) // 256 * 256
     assert ops.loong_attn_workspace_size(fused, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
     assert ops.loong_attn_workspace_size(step, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
     bad = _desc(hq=30)
@@ -100,8 +103,9 @@ def test_workspace_sizes(loong_lib):
 def test_null_pointers_rejected_before_any_cuda_call(loong_lib):
     d = _desc()
     L = ops.lib()
-    assert L.loong_attn_fwd(ctypes.byref(d), None, None, None, None, None, None, 0, None) == \
+    assert L.loong_attn_fwd(ctypes.byref(d), None, None, None, None, None, None, None, 0, None) == \
         ops.LOONG_ERR_INVALID_ARG
+    assert L.loong_attn_bwd(ctypes.byref(d), *([None] * 11), 0, None) == ops.LOONG_ERR_INVALID_ARG
     assert L.loong_lse_merge(10, 3, 2, None, None, None, None, 0, None) == ops.LOONG_ERR_INVALID_ARG
     assert L.loong_lse_merge(0, 128, 2, None, None, None, None, 0, None) == ops.LOONG_OK
     assert L.loong_headctx_pack(1, 2, 3, 4, 8, 128, 0, 0, None, None, None) == \
@@ -127,7 +131,7 @@ def test_rank_major_view_rows_must_fit_int32(loong_lib):
 def test_fwd_ranks_validation_before_any_cuda_call(loong_lib):
     L = ops.lib()
     d = _desc()
-    args = (None,) * 6
+    args = (None,) * 5 + (None, 0, None)   # q, k, v, o, lse, ws, ws_bytes, stream
     for lo, hi in ((-1, 2), (3, 3), (4, 2), (0, d.cp + 1)):
         assert L.loong_attn_fwd_ranks(ctypes.byref(d), lo, hi, *args) == ops.LOONG_ERR_INVALID_ARG
     assert L.loong_attn_fwd_ranks(ctypes.byref(d), 0, 1, *args) == ops.LOONG_ERR_INVALID_ARG  # null tensors
@@ -165,8 +169,9 @@ def test_two_ring_copy_mode_needs_paired_blocks(loong_lib):
 
 @pytest.mark.parametrize("layout", [ops.LAYOUT_NATURAL, ops.LAYOUT_RANK_MAJOR])
 def test_2d_host_workspace_sizes(loong_lib, layout):
-    """Two slots of natural inputs, the natural outputs and LSE, the rank-major
-    tensors (RANK_MAJOR only) and the ring workspaces, each 256-byte aligned."""
+    """Two slots of natural inputs, the natural outputs and LSE, the forward's
+    residual of O (fwd+bwd), the rank-major tensors (RANK_MAJOR only) and the
+    ring workspaces, each 256-byte aligned."""
     w = inputs.WORKLOADS["llama3-8b-s128k"]
     d = ops.make_desc(w, ops.MODE_FUSED, layout=layout)
     up = lambda x: (x + 255) // 256 * 256
@@ -176,7 +181,8 @@ def test_2d_host_workspace_sizes(loong_lib, layout):
     rm = layout == ops.LAYOUT_RANK_MAJOR
     fwd = 2 * (up(qb) + 2 * up(kvb)) + up(qb) + up(lse) + (up(qb) + 2 * up(kvb) + up(qb) if rm else 0)
     both = 2 * (2 * up(qb) + 2 * up(kvb)) + 2 * up(qb) + 2 * up(kvb) + up(lse) + \
-        ((3 * up(qb) + 2 * up(kvb)) + (up(qb) + 2 * up(kvb)) if rm else 0) + ops.loong_attn_workspace_size(d, 1)
+        ((3 * up(qb) + 2 * up(kvb)) + (up(qb) + 2 * up(kvb)) if rm else 0) + up(qb) + \
+        ops.loong_attn_workspace_size(d, 0) + ops.loong_attn_workspace_size(d, 1)
     assert ops.loong_attn_2d_host_workspace_size(d, 0) == fwd + ops.loong_attn_workspace_size(d, 0)
     assert ops.loong_attn_2d_host_workspace_size(d, 1) == both
     assert ops.loong_attn_2d_host_workspace_size(d, 2) == 0
@@ -223,3 +229,16 @@ def test_headctx_pack_n_validation_before_any_cuda_call(loong_lib):
     mis = (P_ * 4)(16, 40, 48, 64)                                            # 8-byte aligned only
     assert call(4, heads, mis, ptrs) == ops.LOONG_ERR_INVALID_ARG
     assert L.loong_headctx_pack_n(4, 0, 4, 2, 128, heads, 128, 0, 1, ptrs, ptrs, None) == ops.LOONG_OK  # empty
+
+
+def test_noalloc_scratch_example_fits(loong_lib):
+    """The header's example for the allocation-free backward (S = 4096,
+    Hq = 8, Hkv = 1, d = 128, FUSED) fits its 32 MiB array, within the header's
+    bound."""
+    w = inputs.Workload("example", 4096, 8, 1, 128, 1, 4, 2, 2, True)
+    need = ops.loong_attn_workspace_size(ops.make_desc(w), 1)
+    assert need <= ops.NOALLOC_SCRATCH_BYTES
+    nblocks = 2 * w.cp
+    estimate = 4 * w.seqlen * w.hq * 128 + 8 * w.seqlen * w.hkv * 128 + 8 * w.hq * (w.seqlen + 3 * nblocks + 128)
+    assert estimate - 8 * w.hq * 3 * nblocks <= need <= estimate + 4 * 256   # block padding, 256-byte rounding
+    assert abs(need / 2 ** 20 - 20.3) < 0.05

@@ -1,8 +1,10 @@
 """Backward parity: dQ, dK, dV of the CUDA ring-attention backward against the
-float64 oracle's gradient on the same seeded bf16 inputs (atol 5e-2 / rtol
-5e-2), plus the gradient-sum invariants.  Both sides form D = rowsum(dO * O)
-from the forward's output rounded to bf16 (the oracle rounds its own float64
-O), the tensor the forward returns."""
+float64 oracle's exact gradient on the same seeded bf16 inputs (atol 5e-2 /
+rtol 5e-2), plus the gradient-sum invariants.  The CUDA backward forms
+D = rowsum(dO * O) from O and the forward's rounding residual of O; the oracle
+from its own float64 O.  Without the residual the library forms D from the
+bf16 O alone: that path is checked against the oracle's D from O rounded to
+bf16, the tensor the forward returns."""
 import numpy as np
 import pytest
 
@@ -32,23 +34,19 @@ def _workload(name):
     return inputs.Workload(name, S, hq, hkv, d, hp, cp, inner, outer, True, placement=pl, batch=B)
 
 
-def _run(w, mode):
+def _run(w, mode, res=True):
     x = inputs.make_inputs(w, device="cuda")
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
-    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], mode=mode)
+    o, lse, o_res = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode, res=res)
+    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=o_res, mode=mode)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     return x, (dq, dk, dv)
 
 
-@pytest.mark.parametrize("mode", [ops.MODE_FUSED, ops.MODE_STEPWISE])
-@pytest.mark.parametrize("name", list(CASES))
-def test_backward_matches_oracle(cuda_device, name, mode):
-    w = _workload(name)
-    x, grads = _run(w, mode)
+def _check_against_oracle(w, x, grads, d_from_bf16_o):
     errors = []
     for b in range(w.batch):
         want = attention.attention_backward(to64(x["q"][b]), to64(x["k"][b]), to64(x["v"][b]),
-                                            to64(x["do"][b]), d_from_bf16_o=True)[:3]
+                                            to64(x["do"][b]), d_from_bf16_o=d_from_bf16_o)[:3]
         for nm, got, exp in zip(("dQ", "dK", "dV"), grads, want):
             try:
                 assert_close(nm, to64(got[b]), exp, ATOL, RTOL)
@@ -57,11 +55,29 @@ def test_backward_matches_oracle(cuda_device, name, mode):
     assert not errors, "\n".join(errors)
 
 
+@pytest.mark.parametrize("mode", [ops.MODE_FUSED, ops.MODE_STEPWISE])
+@pytest.mark.parametrize("name", list(CASES))
+def test_backward_matches_oracle(cuda_device, name, mode):
+    w = _workload(name)
+    x, grads = _run(w, mode)
+    _check_against_oracle(w, x, grads, d_from_bf16_o=False)
+
+
+@pytest.mark.parametrize("name", ["tiny-gqa-s1k", "d128-double-ring", "g8-cp8"])
+def test_backward_without_residual_matches_bf16_o_oracle(cuda_device, name):
+    """No residual: D from the bf16 O, as the oracle's d_from_bf16_o reading."""
+    w = _workload(name)
+    x, grads = _run(w, ops.MODE_FUSED, res=False)
+    _check_against_oracle(w, x, grads, d_from_bf16_o=True)
+
+
 def test_backward_gradient_sums(cuda_device):
     w = _workload("g8-cp8")
     x, (dq, dk, dv) = _run(w, ops.MODE_FUSED)
     G = w.hq // w.hkv
-    dk_sum = to64(dk[0]).sum(axis=0)                 # sum over keys: 0
-    assert np.abs(dk_sum).max() < 0.5, np.abs(dk_sum).max()
+    # sum over keys: scale * sum_i (D_exact,i - D_i) q_i, 0 when D is exact;
+    # what remains is the bf16 rounding of S dK values of magnitude ~1
+    dk_sum = to64(dk[0]).sum(axis=0)
+    assert np.abs(dk_sum).max() < 0.25, np.abs(dk_sum).max()
     do_grp = to64(x["do"][0]).reshape(w.seqlen, w.hkv, G, w.head_dim).sum(axis=(0, 2))
     assert_close("sum dV", to64(dv[0]).sum(axis=0), do_grp, 1.0, 1e-2)

@@ -27,12 +27,12 @@ def _library(path):
 
 def _pass(w, x, mode, layout):
     t = {n: _pack(w, x[n]) for n in ("q", "k", "v", "do")} if layout == ops.LAYOUT_RANK_MAJOR else x
-    o, lse = ops.attn_fwd(w, t["q"], t["k"], t["v"], mode=mode, layout=layout)
-    dq, dk, dv = ops.attn_bwd(w, t["q"], t["k"], t["v"], o, lse, t["do"], mode=mode, layout=layout)
+    o, lse, r = ops.attn_fwd(w, t["q"], t["k"], t["v"], mode=mode, layout=layout)
+    dq, dk, dv = ops.attn_bwd(w, t["q"], t["k"], t["v"], o, lse, t["do"], o_res=r, mode=mode, layout=layout)
     st = ops.loong_get_device_status()
     if layout == ops.LAYOUT_RANK_MAJOR:
-        o, dq, dk, dv = (_unpack(w, a) for a in (o, dq, dk, dv))
-    return st, (o, lse, dq, dk, dv)
+        o, dq, dk, dv, r = (_unpack(w, a) for a in (o, dq, dk, dv, r))
+    return st, (o, lse, dq, dk, dv, r)
 
 
 @pytest.mark.parametrize("mode,layout", [(ops.MODE_FUSED, ops.LAYOUT_NATURAL),
@@ -48,7 +48,7 @@ def test_checked_library_trips_no_check_and_agrees(cuda_device, name, mode, layo
     with _library(ops.CHECKED_LIB_PATH):
         st, got = _pass(w, x, mode, layout)
     assert st == ops.LOONG_OK, "an address check failed"
-    for i in (0, 1, 3, 4):   # O, LSE, dK, dV
+    for i in (0, 1, 3, 4, 5):   # O, LSE, dK, dV, O's residual
         assert torch.equal(got[i], want[i]), i
     assert _within_one_bf16_spacing(got[2], want[2])
 
@@ -63,9 +63,10 @@ def test_checked_library_non_causal_and_rank_forward(cuda_device, name):
         st, got = _pass(w, x, ops.MODE_FUSED, ops.LAYOUT_NATURAL)
         assert st == ops.LOONG_OK
         desc = ops.make_desc(w)
+        ws = ops.workspace(desc, 0)
         o = torch.full_like(x["q"], float("nan"))
         lse = torch.full((w.batch, w.hq, w.seqlen), float("nan"), device="cuda")
         for c in range(w.cp):
-            ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse)
+            ops.loong_attn_fwd_ranks(desc, c, c + 1, x["q"], x["k"], x["v"], o, lse, ws)
         assert ops.loong_get_device_status() == ops.LOONG_OK
     assert torch.equal(got[0], want[0]) and torch.equal(o, want[0]) and torch.equal(lse, want[1])

@@ -23,7 +23,7 @@ def test_expired_wait_reports_timeout_and_context_survives(cuda_device):
     assert ops.loong_get_device_status() == ops.LOONG_OK        # reading cleared the word
     w = inputs.WORKLOADS["tiny-gqa-s1k"]
     x = inputs.make_inputs(w, device="cuda", with_do=False)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"])
     assert ops.loong_get_device_status() == ops.LOONG_OK
     want_o, want_lse = attention.attention_forward(to64(x["q"][0]), to64(x["k"][0]), to64(x["v"][0]))
     assert_close("O", to64(o[0]), want_o, 2e-2, 2e-2)
@@ -43,13 +43,16 @@ def test_host_memory_is_refused_before_any_work(cuda_device):
     lse = torch.full((w.batch, w.hq, w.seqlen), 7.0, device="cuda")
     for host in (x["q"].cpu().pin_memory(), x["q"].cpu()):
         with pytest.raises(ops.LoongError) as e:
-            ops.loong_attn_fwd(desc, host, x["k"], x["v"], o, lse, ws0)
+            ops.loong_attn_fwd(desc, host, x["k"], x["v"], o, lse, None, ws0)
         assert e.value.status == ops.LOONG_ERR_INVALID_ARG
         with pytest.raises(ops.LoongError) as e:
-            ops.loong_attn_fwd(desc, x["q"], x["k"], x["v"], o, lse.cpu().pin_memory(), ws0)
+            ops.loong_attn_fwd(desc, x["q"], x["k"], x["v"], o, lse.cpu().pin_memory(), None, ws0)
+        assert e.value.status == ops.LOONG_ERR_INVALID_ARG
+        with pytest.raises(ops.LoongError) as e:   # the residual output too
+            ops.loong_attn_fwd(desc, x["q"], x["k"], x["v"], o, lse, host, ws0)
         assert e.value.status == ops.LOONG_ERR_INVALID_ARG
         with pytest.raises(ops.LoongError) as e:
-            ops.loong_attn_bwd(desc, x["q"], x["k"], x["v"], o, lse, x["do"], host, x["k"].clone(),
+            ops.loong_attn_bwd(desc, x["q"], x["k"], x["v"], o, None, lse, x["do"], host, x["k"].clone(),
                                x["v"].clone(), ws1)
         assert e.value.status == ops.LOONG_ERR_INVALID_ARG
         with pytest.raises(ops.LoongError) as e:

@@ -1,6 +1,8 @@
 """Forward parity: the CUDA ring-attention forward against the float64 oracle,
 element by element, on seeded bf16 inputs (O within atol 2e-2 / rtol 2e-2,
-LSE within 1e-3 absolute)."""
+LSE within 1e-3 absolute).  O + o_res, the forward's fp32 result before its
+bf16 rounding, is checked ten times tighter: the P V product takes fp16
+probabilities (unit roundoff 2^-11) with fp32 accumulation."""
 import numpy as np
 import pytest
 import torch
@@ -45,7 +47,7 @@ def _oracle(w, x):
 def test_forward_matches_oracle(cuda_device, name, mode):
     w = _workload(name)
     x = inputs.make_inputs(w, device="cuda", with_do=False)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     want_o, want_lse = _oracle(w, x)
     assert_close("O", to64(o), want_o, O_ATOL, O_RTOL)
@@ -56,7 +58,7 @@ def test_chunked_oracle_agrees_on_gpu_inputs(cuda_device):
     """The GPU result also matches the second (ring-walking) oracle."""
     w = _workload("d128-double-ring")
     x = inputs.make_inputs(w, device="cuda", with_do=False)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"])
     ro, rl = ring.ring_forward(to64(x["q"][0]), to64(x["k"][0]), to64(x["v"][0]), w.hp, w.cp,
                                w.ring_inner, w.ring_outer)
     assert_close("O", to64(o[0]), ro, O_ATOL, O_RTOL)
@@ -66,8 +68,8 @@ def test_chunked_oracle_agrees_on_gpu_inputs(cuda_device):
 def test_fused_and_stepwise_agree(cuda_device):
     w = _workload("g8-cp8")
     x = inputs.make_inputs(w, device="cuda", with_do=False)
-    o1, l1 = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=ops.MODE_FUSED)
-    o2, l2 = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=ops.MODE_STEPWISE)
+    o1, l1, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=ops.MODE_FUSED)
+    o2, l2, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=ops.MODE_STEPWISE)
     assert_close("O", to64(o1), to64(o2), 1e-2, 1e-2)
     assert_close("LSE", to64(l1), to64(l2), 1e-4, 0.0)
 
@@ -75,11 +77,11 @@ def test_fused_and_stepwise_agree(cuda_device):
 def test_causal_mask_future_keys_do_not_change_past_rows(cuda_device):
     w = _workload("d128-double-ring")
     x = inputs.make_inputs(w, device="cuda", with_do=False)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"])
     k2, v2 = x["k"].clone(), x["v"].clone()
     k2[:, 700:] = torch.randn_like(k2[:, 700:], dtype=torch.float32).to(torch.bfloat16) * 4
     v2[:, 700:] = 7.0
-    o2, lse2 = ops.attn_fwd(w, x["q"], k2, v2)
+    o2, lse2, _ = ops.attn_fwd(w, x["q"], k2, v2)
     # rows before 700 see identical keys in an identical order: bit-identical
     assert torch.equal(o[:, :700], o2[:, :700])
     assert torch.equal(lse[:, :, :700], lse2[:, :, :700])
@@ -89,9 +91,46 @@ def test_causal_mask_future_keys_do_not_change_past_rows(cuda_device):
 def test_row_zero_returns_its_value_row(cuda_device):
     w = _workload("tiny-gqa-s1k")
     x = inputs.make_inputs(w, device="cuda", with_do=False)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"])
     G = w.hq // w.hkv
     for h in range(w.hq):
         assert torch.equal(o[0, 0, h], x["v"][0, 0, h // G])
         s = (to64(x["q"][0, 0, h]) @ to64(x["k"][0, 0, h // G])) / np.sqrt(w.head_dim)
         assert abs(float(lse[0, h, 0]) - s) < LSE_ATOL
+
+
+@pytest.mark.parametrize("name", ["tiny-gqa-s1k", "d128-double-ring", "ragged-blocks", "g8-cp8"])
+@pytest.mark.parametrize("mode", [ops.MODE_FUSED, ops.MODE_STEPWISE])
+def test_output_residual_carries_the_unrounded_output(cuda_device, name, mode):
+    """o_res = bf16(O32 - bf16(O32)): at most half a bf16 spacing of O, and
+    O + o_res is O32, within 2e-3 of exact attention."""
+    w = _workload(name)
+    x = inputs.make_inputs(w, device="cuda", with_do=False)
+    o, lse, r = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    o64, r64 = to64(o), to64(r)
+    assert np.all(np.abs(r64) <= 2.0 ** -8 * np.abs(o64) + 1e-30)
+    want_o, _ = _oracle(w, x)
+    assert_close("O + o_res", o64 + r64, want_o, 2e-3, 2e-3)
+    # the forward without the residual writes the same O and LSE
+    o2, lse2, none = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode, res=False)
+    assert none is None and torch.equal(o2, o) and torch.equal(lse2, lse)
+
+
+@pytest.mark.parametrize("exp2", [20, -20])
+def test_values_beyond_fp16_range_are_scaled(cuda_device, exp2):
+    """V * 2^20 lies far beyond fp16's range and V * 2^-20 far below its normal
+    range: the forward stores V * 2^-e in fp16 with its largest value in
+    [2^14, 2^15) and multiplies O by 2^e (exact), so O follows V's scale at full
+    precision and LSE does not change at all."""
+    w = _workload("d128-double-ring")
+    x = inputs.make_inputs(w, device="cuda", with_do=False)
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    v2 = x["v"] * (2.0 ** exp2)          # exact in bf16
+    o2, lse2, r2 = ops.attn_fwd(w, x["q"], x["k"], v2)
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    assert torch.equal(lse2, lse)
+    assert torch.isfinite(o2.float()).all()
+    want_o, _ = _oracle(w, x)
+    scaled = (to64(o2) + to64(r2)) * 2.0 ** -exp2
+    assert_close("O(V * 2^k) * 2^-k", scaled, want_o, 2e-3, 2e-3)

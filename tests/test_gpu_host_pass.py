@@ -24,17 +24,17 @@ GATHER = {1: 1, 0: 2}
 def _device_pass(w, x, layout, mode=ops.MODE_FUSED):
     """The same pass through the device entry points: (o, lse, dq, dk, dv)."""
     if layout == ops.LAYOUT_NATURAL:
-        o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
+        o, lse, r = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
         if not w.backward:
             return o, lse
-        return (o, lse) + ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], mode=mode)
+        return (o, lse) + ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=r, mode=mode)
     g = GATHER[w.placement]
     p = {n: ops.headctx_pack(t, w.cp, w.hp, g) for n, t in x.items()}
-    o, lse = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=layout)
+    o, lse, r = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=layout)
     un = lambda t: ops.headctx_unpack(t, w.batch, w.cp, w.hp, g)
     if not w.backward:
         return un(o), lse
-    dq, dk, dv = ops.attn_bwd(w, p["q"], p["k"], p["v"], o, lse, p["do"], mode=mode, layout=layout)
+    dq, dk, dv = ops.attn_bwd(w, p["q"], p["k"], p["v"], o, lse, p["do"], o_res=r, mode=mode, layout=layout)
     return un(o), lse, un(dq), un(dk), un(dv)
 
 
@@ -103,7 +103,7 @@ def test_host_pass_matches_oracle(cuda_device):
     want_o, want_lse = attention.attention_forward(q, k, v)
     assert_close("O", to64(hout["o"][0]), want_o, 2e-2, 2e-2)
     assert_close("LSE", to64(hout["lse"][0]), want_lse, 1e-3, 0.0)
-    g = attention.attention_backward(q, k, v, do, d_from_bf16_o=True)[:3]
+    g = attention.attention_backward(q, k, v, do)[:3]
     for n, exp in zip(("dq", "dk", "dv"), g):
         assert_close(n, to64(hout[n][0]), exp, 5e-2, 5e-2)
 

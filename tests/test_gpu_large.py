@@ -9,19 +9,22 @@ times (FUSED mode): the oracle recomputes sampled outputs one by one.
     query heads (rows of dS sum to 0, rows of P to 1).
 Parity beyond these samples rests on the small-size element-wise tests.
 
-dQ and dK carry the term -scale * D * (P-weighted keys or queries), with
-D = rowsum(dO * O) formed from the forward's O, itself built from bf16
-probabilities and rounded to bf16.  With the 1 % keys x8 of the 1M workload that
-term amplifies the bf16 rounding beyond 5e-2 on a few elements, so the test
-adds the oracle's first-order bound on it (attention.d_rounding_bounds) to the
-stated atol / rtol; the bound is computed from oracle quantities only.
+The tolerances are the stated ones (O 2e-2, LSE 1e-3, dQ/dK/dV 5e-2) with no
+allowance on top, against the oracle's exact gradient (D from its float64 O).
+dQ and dK carry the term -scale * D * (P-weighted keys or queries); with the
+1 % keys x8 of the 1M workload that term amplifies any error in D, so the
+library forms D from O and the forward's rounding residual of O (fp16
+probabilities in the forward's P V product), which keeps it well inside.
+
+The head-context repack at the 70B layer's full size is pinned to the oracle's
+index map (sampled output rows, bit for bit) and its inverse to the identity.
 """
 import numpy as np
 import pytest
 import torch
 
 from head_context_attention_gb300 import inputs, ops
-from oracle import attention
+from oracle import attention, repack, schedule
 from tests.helpers import assert_close
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -51,9 +54,9 @@ def _head_arrays(x, key, heads):
 def test_full_size_sampled_parity(cuda_device, name):
     w = inputs.WORKLOADS[name]
     x = inputs.make_inputs(w, device="cuda", with_do=True)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    o, lse, o_res = ops.attn_fwd(w, x["q"], x["k"], x["v"])
     if w.backward:
-        dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"])
+        dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=o_res)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     rng = np.random.default_rng(7)
     rows = _sample_rows(w, rng)
@@ -70,9 +73,8 @@ def test_full_size_sampled_parity(cuda_device, name):
         assert_close(f"LSE h{h}", f64(lse[0, h, rows]), rl[0], 1e-3, 0.0)
         if w.backward:
             do = f64(x["do"][0, :, h:h + 1])
-            rdq, dbound = attention.attention_backward_rows(q, k, v, do, rows, [0], d_from_bf16_o=True,
-                                                            with_d_bound=True)
-            assert_close(f"dQ h{h}", f64(dq[0, rows, h]), rdq[0], 5e-2, 5e-2, extra=dbound[0])
+            rdq = attention.attention_backward_rows(q, k, v, do, rows, [0])
+            assert_close(f"dQ h{h}", f64(dq[0, rows, h]), rdq[0], 5e-2, 5e-2)
     if not w.backward:
         return
     # sampled keys of the last kv head, from the tail of the sequence
@@ -85,9 +87,8 @@ def test_full_size_sampled_parity(cuda_device, name):
     do = f64(x["do"][0, :, qh])
     k = f64(x["k"][0, :, g:g + 1])
     v = f64(x["v"][0, :, g:g + 1])
-    sk, sv, kbound = attention.attention_backward_keys(q, k, v, do, keys, kv_head=0, d_from_bf16_o=True,
-                                                       with_d_bound=True)
-    assert_close("dK keys", f64(dk[0, keys, g]), sk, 5e-2, 5e-2, extra=kbound)
+    sk, sv = attention.attention_backward_keys(q, k, v, do, keys, kv_head=0)
+    assert_close("dK keys", f64(dk[0, keys, g]), sk, 5e-2, 5e-2)
     assert_close("dV keys", f64(dv[0, keys, g]), sv, 5e-2, 5e-2)
     # Invariants over every key.  The stored bf16 values each carry a rounding
     # error of at most half a bf16 spacing (<= 2^-8 |x|), independent across
@@ -95,12 +96,11 @@ def test_full_size_sampled_parity(cuda_device, name):
     # sqrt(sum x^2); the bound is 6 sigma plus 1e-3 relative.
     def noise(t):
         return 6.0 * 2.0 ** -7 / np.sqrt(12.0) * np.sqrt((t[0].double() ** 2).sum(dim=0).cpu().numpy())
-    # sum_j dK_j = scale * sum_i (D_exact,i - D_i) q_i: zero only when D is exact.
-    # With peaky keys the D formed from the returned O moves it well beyond
-    # rounding noise (see the module docstring), so it is checked elsewhere.
-    if w.peaky_keys == 0:
-        dk_sum = dk[0].double().sum(dim=0).cpu().numpy()
-        assert np.all(np.abs(dk_sum) <= noise(dk) + 1e-3), np.abs(dk_sum).max()
+    # sum_j dK_j = scale * sum_i (D_exact,i - D_i) q_i: zero when D is exact,
+    # for every workload (the peaky one included)
+    dk_sum = dk[0].double().sum(dim=0).cpu().numpy()
+    dk_bound = noise(dk) + 1e-3
+    assert np.all(np.abs(dk_sum) <= dk_bound), (np.abs(dk_sum).max(), float((np.abs(dk_sum) / dk_bound).max()))
     do_grp = x["do"][0].double().reshape(w.seqlen, w.hkv, G, w.head_dim).sum(dim=(0, 2)).cpu().numpy()
     dv_sum = dv[0].double().sum(dim=0).cpu().numpy()
     err = np.abs(dv_sum - do_grp)
@@ -122,13 +122,13 @@ def test_full_size_bench_pass_equals_natural(cuda_device):
     LSE, dK, dV bit for bit, dQ up to its fp32 reduction order."""
     w = inputs.WORKLOADS["llama3-8b-s128k"]
     x = inputs.make_inputs(w, device="cuda", with_do=True)
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"])
-    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"])
+    o, lse, r = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=r)
     p = {n: ops.headctx_pack(x[n], w.cp, w.hp, 1) for n in ("q", "k", "v", "do")}
     del x
     rm = ops.LAYOUT_RANK_MAJOR
-    o2, lse2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], layout=rm)
-    dq2, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], layout=rm)
+    o2, lse2, r2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], layout=rm)
+    dq2, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], o_res=r2, layout=rm)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     un = lambda t: ops.headctx_unpack(t, w.batch, w.cp, w.hp, 1)
     assert torch.equal(lse2, lse)
@@ -136,3 +136,42 @@ def test_full_size_bench_pass_equals_natural(cuda_device):
     assert torch.equal(un(dk2), dk)
     assert torch.equal(un(dv2), dv)
     assert _within_one_bf16_spacing(un(dq2), dq)
+
+
+def test_full_size_repack_pinned_to_oracle_index_map(cuda_device):
+    """The 70B layer's repack (S = 262144, Hq = 64 and Hkv = 8 heads, P = hp = 8,
+    cp = 32 paired blocks), Q, K, V in one loong_headctx_pack_n launch.  The
+    oracle's own repack, applied to a tensor of (token, head) ids, gives the
+    source of every output row; >= 4096 sampled rows of each output (among them
+    the first and last token of every block) must equal their sources bit for
+    bit.  The inverse repack must give back each input bit for bit."""
+    w = inputs.WORKLOADS["llama3-70b-s256k"]
+    x = inputs.make_inputs(w, device="cuda", with_do=False)
+    s_local = w.seqlen // (w.cp * w.hp)
+    names = ("q", "k", "v")
+    heads = [w.hq, w.hkv, w.hkv]
+    outs = [torch.empty((w.batch * w.cp, w.hp, w.seqlen // w.cp, h // w.hp, w.head_dim), dtype=torch.bfloat16,
+                        device="cuda") for h in heads]
+    ops.loong_headctx_pack_n([x[n] for n in names], outs, w.batch, w.cp, w.hp, s_local, heads, w.head_dim, 0, 1)
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    rng = np.random.default_rng(11)
+    S, blk, chunk = w.seqlen, w.seqlen // (2 * w.cp), w.seqlen // w.cp
+    for n, H, y in zip(names, heads, outs):
+        ids = (np.arange(S)[:, None] * H + np.arange(H)[None, :]).reshape(S, H, 1)
+        src = repack.headctx_pack(ids, w.cp, w.hp, schedule.ZIGZAG)        # [cp, P, S/cp, H/P, 1]
+        # rows (c, p, r): every block's first and last token, then random ones
+        rows = {(c, p, r) for c in range(w.cp) for p in range(w.hp) for r in (0, blk - 1, blk, chunk - 1)}
+        while len(rows) < 4096 + 4 * w.cp * w.hp:
+            rows.add((int(rng.integers(w.cp)), int(rng.integers(w.hp)), int(rng.integers(chunk))))
+        c, p, r = (np.array(a) for a in zip(*sorted(rows)))
+        got = y[torch.as_tensor(c, device="cuda"), torch.as_tensor(p, device="cuda"),
+                torch.as_tensor(r, device="cuda")].view(torch.int16).cpu().numpy()     # [rows, H/P, d]
+        sid = src[c, p, r, :, 0]                                                      # [rows, H/P]
+        tok, head = torch.as_tensor(sid // H, device="cuda"), torch.as_tensor(sid % H, device="cuda")
+        want = x[n][0][tok, head].view(torch.int16).cpu().numpy()                    # [rows, H/P, d]
+        assert np.array_equal(got, want), n
+    backs = [torch.empty_like(x[n]) for n in names]
+    ops.loong_headctx_pack_n(outs, backs, w.batch, w.cp, w.hp, s_local, heads, w.head_dim, 1, 1)
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    for n, b in zip(names, backs):
+        assert torch.equal(b, x[n]), n

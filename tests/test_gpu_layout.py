@@ -50,14 +50,15 @@ def _within_one_bf16_spacing(a, b):
 def test_rank_major_path_equals_natural(cuda_device, name, mode):
     w = _workload(name)
     x = inputs.make_inputs(w, device="cuda", with_do=True)
-    o_n, lse_n = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
-    dq_n, dk_n, dv_n = ops.attn_bwd(w, x["q"], x["k"], x["v"], o_n, lse_n, x["do"], mode=mode)
+    o_n, lse_n, r_n = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
+    dq_n, dk_n, dv_n = ops.attn_bwd(w, x["q"], x["k"], x["v"], o_n, lse_n, x["do"], o_res=r_n, mode=mode)
     p = {n: _pack(w, x[n]) for n in ("q", "k", "v", "do")}
-    o_p, lse_p = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=ops.LAYOUT_RANK_MAJOR)
-    dq_p, dk_p, dv_p = ops.attn_bwd(w, p["q"], p["k"], p["v"], o_p, lse_p, p["do"], mode=mode,
+    o_p, lse_p, r_p = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=ops.LAYOUT_RANK_MAJOR)
+    dq_p, dk_p, dv_p = ops.attn_bwd(w, p["q"], p["k"], p["v"], o_p, lse_p, p["do"], o_res=r_p, mode=mode,
                                     layout=ops.LAYOUT_RANK_MAJOR)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     assert torch.equal(_unpack(w, o_p), o_n)
+    assert torch.equal(_unpack(w, r_p), r_n)
     assert torch.equal(lse_p, lse_n)
     assert torch.equal(_unpack(w, dk_p), dk_n)
     assert torch.equal(_unpack(w, dv_p), dv_n)
@@ -68,14 +69,14 @@ def test_rank_major_path_matches_oracle(cuda_device):
     w = _workload("d128-double-ring")
     x = inputs.make_inputs(w, device="cuda", with_do=True)
     p = {n: _pack(w, x[n]) for n in ("q", "k", "v", "do")}
-    o_p, lse_p = ops.attn_fwd(w, p["q"], p["k"], p["v"], layout=ops.LAYOUT_RANK_MAJOR)
-    dq_p, dk_p, dv_p = ops.attn_bwd(w, p["q"], p["k"], p["v"], o_p, lse_p, p["do"],
+    o_p, lse_p, r_p = ops.attn_fwd(w, p["q"], p["k"], p["v"], layout=ops.LAYOUT_RANK_MAJOR)
+    dq_p, dk_p, dv_p = ops.attn_bwd(w, p["q"], p["k"], p["v"], o_p, lse_p, p["do"], o_res=r_p,
                                     layout=ops.LAYOUT_RANK_MAJOR)
     q, k, v, do = (to64(x[n][0]) for n in ("q", "k", "v", "do"))
     want_o, want_lse = attention.attention_forward(q, k, v)
     assert_close("O", to64(_unpack(w, o_p)[0]), want_o, 2e-2, 2e-2)
     assert_close("LSE", to64(lse_p[0]), want_lse, 1e-3, 0.0)
-    dq, dk, dv = attention.attention_backward(q, k, v, do, d_from_bf16_o=True)[:3]
+    dq, dk, dv = attention.attention_backward(q, k, v, do)[:3]
     assert_close("dQ", to64(_unpack(w, dq_p)[0]), dq, 5e-2, 5e-2)
     assert_close("dK", to64(_unpack(w, dk_p)[0]), dk, 5e-2, 5e-2)
     assert_close("dV", to64(_unpack(w, dv_p)[0]), dv, 5e-2, 5e-2)
@@ -97,11 +98,12 @@ def test_fwd_ranks_union_is_the_full_forward(cuda_device, name, layout):
     x = inputs.make_inputs(w, device="cuda", with_do=False)
     if layout == ops.LAYOUT_RANK_MAJOR:
         x = {n: _pack(w, x[n]) for n in ("q", "k", "v")}
-    o_full, lse_full = ops.attn_fwd(w, x["q"], x["k"], x["v"], layout=layout)
+    o_full, lse_full, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"], layout=layout, res=False)
     desc = ops.make_desc(w, layout=layout)
+    ws = ops.workspace(desc, 0)
     o = torch.full_like(o_full, float("nan"))
     lse = torch.full_like(lse_full, float("nan"))
-    ops.loong_attn_fwd_ranks(desc, 0, 1, x["q"], x["k"], x["v"], o, lse)
+    ops.loong_attn_fwd_ranks(desc, 0, 1, x["q"], x["k"], x["v"], o, lse, ws)
     torch.cuda.synchronize()
     # rank 0's rows are written, every other row untouched
     assert torch.equal(_rank_rows(w, layout, o, 0), _rank_rows(w, layout, o_full, 0))
@@ -113,7 +115,7 @@ def test_fwd_ranks_union_is_the_full_forward(cuda_device, name, layout):
     for c in range(1, w.cp):
         assert bool(_rank_rows(w, layout, o, c).isnan().all())
     if w.cp > 1:
-        ops.loong_attn_fwd_ranks(desc, 1, w.cp, x["q"], x["k"], x["v"], o, lse)
+        ops.loong_attn_fwd_ranks(desc, 1, w.cp, x["q"], x["k"], x["v"], o, lse, ws)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     assert torch.equal(o, o_full)
     assert torch.equal(lse, lse_full)
@@ -134,12 +136,13 @@ def test_stepwise_copy_equals_stepwise(cuda_device, name):
     # the two-ring variant needs two blocks per rank (paired placement)
     modes = [ops.MODE_STEPWISE, ops.MODE_STEPWISE_COPY] + ([ops.MODE_STEPWISE_COPY_AB] if w.placement == 1 else [])
     for mode in modes:
-        o, lse = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=rm)
-        res[mode] = (o, lse) + ops.attn_bwd(w, p["q"], p["k"], p["v"], o, lse, p["do"], mode=mode, layout=rm)
+        o, lse, r = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=rm)
+        res[mode] = (o, lse) + ops.attn_bwd(w, p["q"], p["k"], p["v"], o, lse, p["do"], o_res=r, mode=mode,
+                                            layout=rm) + (r,)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     a = res[ops.MODE_STEPWISE]
     for mode in modes[1:]:
         b = res[mode]
-        for i in (0, 1, 3, 4):   # O, LSE, dK, dV
+        for i in (0, 1, 3, 4, 5):   # O, LSE, dK, dV, O's residual
             assert torch.equal(a[i], b[i]), (mode, i)
         assert _within_one_bf16_spacing(b[2], a[2])

@@ -32,15 +32,15 @@ def _workload(name):
 def test_noncausal_matches_oracle(cuda_device, name, mode):
     w = _workload(name)
     x = inputs.make_inputs(w, device="cuda")
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
-    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], mode=mode)
+    o, lse, r = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
+    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=r, mode=mode)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     for b in range(w.batch):
         q, k, v, do = (to64(x[n][b]) for n in ("q", "k", "v", "do"))
         want_o, want_lse = attention.attention_forward(q, k, v, causal=False)
         assert_close("O", to64(o[b]), want_o, 2e-2, 2e-2)
         assert_close("LSE", to64(lse[b]), want_lse, 1e-3, 0.0)
-        g = attention.attention_backward(q, k, v, do, causal=False, d_from_bf16_o=True)[:3]
+        g = attention.attention_backward(q, k, v, do, causal=False)[:3]
         for nm, got, exp in zip(("dQ", "dK", "dV"), (dq, dk, dv), g):
             assert_close(nm, to64(got[b]), exp, 5e-2, 5e-2)
 
@@ -48,13 +48,13 @@ def test_noncausal_matches_oracle(cuda_device, name, mode):
 def test_noncausal_rank_major_and_copy_mode_equal_natural(cuda_device):
     w = _workload("nc-d128-double-ring")
     x = inputs.make_inputs(w, device="cuda")
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=ops.MODE_STEPWISE)
-    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], mode=ops.MODE_STEPWISE)
+    o, lse, r = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=ops.MODE_STEPWISE)
+    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=r, mode=ops.MODE_STEPWISE)
     p = {n: ops.headctx_pack(x[n], w.cp, w.hp, 1) for n in ("q", "k", "v", "do")}
     rm = ops.LAYOUT_RANK_MAJOR
     un = lambda t: ops.headctx_unpack(t, w.batch, w.cp, w.hp, 1)
     for mode in (ops.MODE_STEPWISE, ops.MODE_STEPWISE_COPY):
-        o2, lse2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=rm)
-        _, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], mode=mode, layout=rm)
-        assert torch.equal(un(o2), o) and torch.equal(lse2, lse)
+        o2, lse2, r2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=mode, layout=rm)
+        _, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], o_res=r2, mode=mode, layout=rm)
+        assert torch.equal(un(o2), o) and torch.equal(lse2, lse) and torch.equal(un(r2), r)
         assert torch.equal(un(dk2), dk) and torch.equal(un(dv2), dv)

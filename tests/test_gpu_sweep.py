@@ -53,24 +53,25 @@ def test_sweep_matches_oracle_and_layouts_agree(cuda_device, c):
                         True, placement=c["placement"], batch=c["batch"], causal=c["causal"])
     assert ops.loong_attn_check(ops.make_desc(w, c["mode"])) == ops.LOONG_OK
     x = inputs.make_inputs(w, device="cuda")
-    o, lse = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=c["mode"])
-    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], mode=c["mode"])
+    o, lse, o_res = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=c["mode"])
+    dq, dk, dv = ops.attn_bwd(w, x["q"], x["k"], x["v"], o, lse, x["do"], o_res=o_res, mode=c["mode"])
     assert ops.loong_get_device_status() == ops.LOONG_OK
     for b in range(w.batch):
         q, k, v, do = (to64(x[n][b]) for n in ("q", "k", "v", "do"))
         want_o, want_lse = attention.attention_forward(q, k, v, causal=c["causal"])
         assert_close("O", to64(o[b]), want_o, 2e-2, 2e-2)
         assert_close("LSE", to64(lse[b]), want_lse, 1e-3, 0.0)
-        g = attention.attention_backward(q, k, v, do, causal=c["causal"], d_from_bf16_o=True)[:3]
+        g = attention.attention_backward(q, k, v, do, causal=c["causal"])[:3]
         for nm, got, exp in zip(("dQ", "dK", "dV"), (dq, dk, dv), g):
             assert_close(nm, to64(got[b]), exp, 5e-2, 5e-2)
     gather = 1 if c["placement"] == 1 else 2
     p = {n: ops.headctx_pack(x[n], w.cp, w.hp, gather) for n in ("q", "k", "v", "do")}
     rm = ops.LAYOUT_RANK_MAJOR
-    o2, lse2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=c["mode"], layout=rm)
-    dq2, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], mode=c["mode"], layout=rm)
+    o2, lse2, r2 = ops.attn_fwd(w, p["q"], p["k"], p["v"], mode=c["mode"], layout=rm)
+    dq2, dk2, dv2 = ops.attn_bwd(w, p["q"], p["k"], p["v"], o2, lse2, p["do"], o_res=r2, mode=c["mode"], layout=rm)
     assert ops.loong_get_device_status() == ops.LOONG_OK
     un = lambda t: ops.headctx_unpack(t, w.batch, w.cp, w.hp, gather)
     assert torch.equal(lse2, lse)
-    assert torch.equal(un(o2), o) and torch.equal(un(dk2), dk) and torch.equal(un(dv2), dv)
+    assert torch.equal(un(o2), o) and torch.equal(un(r2), o_res)
+    assert torch.equal(un(dk2), dk) and torch.equal(un(dv2), dv)
     assert _within_one_bf16_spacing(un(dq2), dq)
