@@ -60,7 +60,17 @@ def parse_args(argv=None):
     p.add_argument("--fwd-only", action="store_true", help="time the forward pass alone")
     p.add_argument("--non-causal", action="store_true",
                    help="every query sees every key (FLOPs counted over all S^2 pairs)")
+    p.add_argument("--configs", action=argparse.BooleanOptionalAction, default=None,
+                   help="after the headline workload, time the other full-size configurations "
+                        "(1 warm-up + 2 steps each); default: on for the default workload at N=1")
     return p.parse_args(argv)
+
+
+# The other configurations timed after the headline one (--configs), and the
+# GB300 dense bf16 tensor-core rate from NVIDIA's datasheet (no sparsity),
+# reported beside the measured peaks.
+OTHER_CONFIGS = ("llama3-8b-s32k-fwd", "llama3-70b-s256k", "headgroup-s1m-peaky")
+DATASHEET_BF16_TFLOPS = 2250.0
 
 
 def measured_peaks():
@@ -367,6 +377,103 @@ def cpu_sample(w, seconds, arrays):
                       f"{el:.1f} s"}
 
 
+# ------------------------------------------------------------------ other configurations
+def time_config(w, dev, stream, peaks, steps=2, warmup=1):
+    """One configuration at full size, the headline's step (rank-major repack in,
+    FUSED ring forward (+ backward), repack out): step and kernel rates.  A
+    workload with the Q/K/V repack in its definition also gets that repack
+    timed alone (one launch, Q, K, V) against 75 % of the measured HBM rate."""
+    import torch
+
+    from head_context_attention_gb300 import inputs, ops
+
+    path = TwoDPath(w, ops.MODE_FUSED, "rank-major", dev, stream)
+    x = inputs.make_inputs(w, device=dev, with_do=w.backward)
+
+    def step():
+        path.pack_in(x)
+        path.fwd(x)
+        path.bwd(x)
+        path.unpack_out()
+
+    for _ in range(warmup):
+        step()
+    mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(steps)]
+    ev_f, ev_b, ev_p, ev_u = mk(), mk(), mk(), mk()
+    for a, b in ev_f + ev_b:
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev_p[i][0].record(stream)
+        path.pack_in(x)
+        ev_p[i][1].record(stream)
+        ops.loong_set_timing_events(*ev_f[i])
+        path.fwd(x)
+        if w.backward:
+            ops.loong_set_timing_events(*ev_b[i])
+            path.bwd(x)
+        ops.loong_set_timing_events(None, None)
+        ev_u[i][0].record(stream)
+        path.unpack_out()
+        ev_u[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ops.loong_get_device_status(stream) != ops.LOONG_OK:
+        raise SystemExit(f"device status after {w.name}")
+    ms = t0.elapsed_time(t1) / steps
+    peak = peaks["bf16_tflops_sustained"]
+    f_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_f)
+    rec = {"seqlen": w.seqlen, "hq": w.hq, "hkv": w.hkv, "hp": w.hp, "cp": w.cp,
+           "ring": f"{w.ring_inner}x{w.ring_outer}", "pass": "fwd+bwd" if w.backward else "fwd",
+           "peaky_keys": w.peaky_keys, "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 3),
+           "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2)}
+    fwd_tf = w.fwd_flops / (f_ms * 1e-3) / 1e12
+    rec["ring_fwd_kernel"] = {"ms": round(f_ms, 3), "tflops": round(fwd_tf, 2), "frac_of_peak": round(fwd_tf / peak, 4)}
+    if w.backward:
+        b_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_b)
+        bwd_tf = 2.5 * w.fwd_flops / (b_ms * 1e-3) / 1e12
+        rec["ring_bwd_kernel"] = {"ms": round(b_ms, 3), "tflops": round(bwd_tf, 2),
+                                  "frac_of_peak": round(bwd_tf / peak, 4)}
+    in_bytes, out_bytes = path.repack_bytes()
+    for key, evs, nbytes in (("headctx_pack_in", ev_p, in_bytes), ("headctx_pack_out", ev_u, out_bytes)):
+        p_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        gbs = nbytes / (p_ms * 1e-3) / 1e9
+        rec[key] = {"ms": round(p_ms, 3), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                    "bytes": nbytes}
+    if w.repack:
+        names = TwoDPath.FWD_IN
+        nbytes = sum(2 * x[n].numel() * x[n].element_size() for n in names)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+        for a, b in ev:
+            a.record(stream)
+            path._pack([x[n] for n in names], [path.kt[n] for n in names], names, 0)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        q_ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        gbs = nbytes / (q_ms * 1e-3) / 1e9
+        rec["qkv_repack"] = {"ms": round(q_ms, 3), "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                             "bytes": nbytes, "target_ms_at_75pct_hbm": round(nbytes / (0.75 * peaks["hbm_gbs"] * 1e9) * 1e3, 3)}
+    del path, x
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_other_configs(names, dev, stream, peaks, local):
+    """Every configuration in `names`, one after the other, under one clock sampler."""
+    from head_context_attention_gb300 import inputs
+
+    out = {}
+    with ClockSampler(local) as clk:
+        for n in names:
+            out[n] = time_config(inputs.WORKLOADS[n], dev, stream, peaks)
+    out["clocks"] = clk.summary()
+    return out
+
+
 # ------------------------------------------------------------------ GPU arm
 class TwoDPath:
     """One fwd+bwd pass of 2D attention through the library's C entry points.
@@ -585,9 +692,12 @@ def run_gpu(args, w, rank, local, world, pg):
                          "of L2); no flush",
                    "flops_per_step": flops_step},
         "pct_of_peak": round(100.0 * tflops / world / peak, 2),
+        "pct_of_datasheet_peak": round(100.0 * tflops / world / DATASHEET_BF16_TFLOPS, 2),
         "roofline": {"bound": "tensor", "kernel": f"ring_{dominant}_kernel", "achieved": round(dom_tf, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(dom_tf / peak, 4),
                      "peak_kind": f"bf16 sustained, of {peaks['source']}",
+                     "frac_of_burst": round(dom_tf / peaks["bf16_tflops"], 4),
+                     "frac_of_datasheet": round(dom_tf / DATASHEET_BF16_TFLOPS, 4),
                      # the record holds FUSED launches (one launch per pass)
                      "traffic": (recorded_traffic(f"ring_{dominant}_kernel", w.name, args.layout)
                                  if mode == ops.MODE_FUSED and w.causal else None),
@@ -761,9 +871,18 @@ def main(argv=None):
 
     rank, local, world, pg = dist_setup(args.gpus)
     result, x = run_gpu(args, w, rank, local, world, pg)
-    if rank == 0 and not args.no_cpu_baseline:
-        arrays = oracle_inputs(w, x)
-        del x
+    arrays = oracle_inputs(w, x) if rank == 0 and not args.no_cpu_baseline else None
+    del x
+    configs = args.configs if args.configs is not None else (args.workload == DEFAULT_WORKLOAD and world == 1
+                                                             and not args.seqlen and not args.fwd_only
+                                                             and not args.non_causal)
+    if configs:
+        import torch
+        torch.cuda.empty_cache()
+        dev = torch.device("cuda", local)
+        result["configs"] = run_other_configs([n for n in OTHER_CONFIGS if n != w.name], dev,
+                                              torch.cuda.current_stream(dev), measured_peaks(), local)
+    if arrays is not None:
         result["cpu_baseline"] = cpu_sample(w, args.cpu_seconds, arrays)
     if rank == 0:
         print(json.dumps(result))

@@ -290,7 +290,6 @@ size_t loong_attn_workspace_size(const loong_attn_desc* d, int pass) {
   if (loong_attn_check(d) != LOONG_OK) return 0;
   const size_t q_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hq * d->head_dim;
   const size_t kv_elems = static_cast<size_t>(d->batch) * d->seqlen * d->hkv * d->head_dim;
-  const size_t rows = static_cast<size_t>(d->batch) * d->hq * d->seqlen;
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   // STEPWISE_COPY: two receive buffers each for K and V, bf16
   const size_t recv = is_copy_mode(*d) ? 4 * up(kv_elems * 2) : 0;

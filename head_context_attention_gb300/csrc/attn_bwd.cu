@@ -269,7 +269,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else if (warp == C::CW + 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err));
+      };
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S^T, dP^T: both K-major
       constexpr uint32_t id_dkv = idesc_bf16(128, D, false, true);   // dV, dK: B MN-major
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // dQ: A and B MN-major
@@ -280,72 +283,72 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
-          mma_ss(tbase + dst, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), id_s,
+          mma_ss_w(tbase + dst, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), id_s,
                  kk > 0);
         }
       };
-      bool ok = mbar_wait(kv_full, 0, abort_flag, a.err) && mbar_wait(&q_full[0], 0, abort_flag, a.err);
+      bool ok = warp_wait(kv_full, 0, abort_flag, a.err) && warp_wait(&q_full[0], 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
         mm_s(C::R0, k_addr, q_addr);
-        mma_commit(s_full);
+        mma_commit_w(s_full);
         mm_s(C::R1, v_addr, o_addr);
-        mma_commit(dp_full);
+        mma_commit_w(dp_full);
         bool fresh = true;  // next dV / dK start a new tensor-memory sum
         for (int i = 0; i < n; ++i) {
           const int s = i % C::NS;
           const uint32_t qs = q_addr + s * C::TILE_BYTES, os = o_addr + s * C::TILE_BYTES;
-          if (!mbar_wait(p_full, i & 1, abort_flag, a.err)) break;
+          if (!warp_wait(p_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           // dV += P^T dO: A = P^T (TMEM: each group's bf16 pairs in the first
           // columns of its own GW, 8 columns per 16 queries), B = dO MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ts(tbase + C::RV,
+            mma_ts_w(tbase + C::RV,
                    tbase + C::R0 + (kk * 16 / C::GW) * C::GW + ((kk * 16 % C::GW) / 32) * 16 + (kk & 1) * 8,
                    sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, !fresh || kk > 0);
-          if (!mbar_wait(ds_full, i & 1, abort_flag, a.err)) break;
+          if (!warp_wait(ds_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           // dQ = dS K: A = dS (dS^T read MN-major), B = K MN-major; first, so
           // the drain of dQ overlaps the dK product
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss(tbase + C::R1, sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024),
+            mma_ss_w(tbase + C::R1, sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024),
                    sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024), id_dq, kk > 0);
-          mma_commit(dq_full);
+          mma_commit_w(dq_full);
           // dK += dS^T Q: A = dS^T K-major (queries contiguous), B = Q MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
-            mma_ss(tbase + C::RK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::ATOM_BYTES, 1024),
+            mma_ss_w(tbase + C::RK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::ATOM_BYTES, 1024),
                    id_dkv, !fresh || kk > 0);
           }
-          mma_commit(dk_done);
+          mma_commit_w(dk_done);
           fresh = false;
           const bool flush = i + 1 < n && (i + 1) % kFlush == 0;
           if (flush) {
-            mma_commit(acc_full);
+            mma_commit_w(acc_full);
             fresh = true;
           }
           if (i + 1 < n) {
             const int s1 = (i + 1) % C::NS;
-            if (!mbar_wait(&q_full[s1], ((i + 1) / C::NS) & 1, abort_flag, a.err)) break;
+            if (!warp_wait(&q_full[s1], ((i + 1) / C::NS) & 1, abort_flag, a.err)) break;
             tc_fence_after();
             mm_s(C::R0, k_addr, q_addr + s1 * C::TILE_BYTES);  // R0's P^T was read by dV(i), issued earlier
-            mma_commit(s_full);
-            if (!mbar_wait(dq_empty, i & 1, abort_flag, a.err)) break;
+            mma_commit_w(s_full);
+            if (!warp_wait(dq_empty, i & 1, abort_flag, a.err)) break;
             tc_fence_after();
             mm_s(C::R1, v_addr, o_addr + s1 * C::TILE_BYTES);
-            mma_commit(dp_full);
+            mma_commit_w(dp_full);
             if (flush) {
-              if (!mbar_wait(acc_empty, ((i + 1) / kFlush - 1) & 1, abort_flag, a.err)) break;
+              if (!warp_wait(acc_empty, ((i + 1) / kFlush - 1) & 1, abort_flag, a.err)) break;
               tc_fence_after();
             }
           }
         }
-        mma_commit(done_bar);
+        mma_commit_w(done_bar);
       }
-      mma_commit(drain);
+      mma_commit_w(drain);
       mbar_drain(drain, 0, a.err);
     }
   } else if (warp == C::CW + 2) {

@@ -216,7 +216,10 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {  // the whole warp runs the loop; one elected lane issues
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err));
+      };
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_f16(128, D, false, true);  // P and V in fp16
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
@@ -226,53 +229,53 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
           const uint64_t da = sdesc_sw128(q_addr + h * C::TILE_BYTES + off, 16, 1024);
           const uint64_t db = sdesc_sw128(k_addr + s * C::TILE_BYTES + off, 16, 1024);
-          mma_ss(tbase + C::S_COL(h), da, db, id_qk, kk > 0);
+          mma_ss_w(tbase + C::S_COL(h), da, db, id_qk, kk > 0);
         }
       };
       auto pv = [&](int h, int s, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t db = sdesc_sw128(v_addr + s * C::TILE_BYTES + kk * 2048, C::ATOM_BYTES, 1024);
-          mma_ts(tbase + C::O_COL(h), tbase + C::S_COL(h) + kk * 8, db, id_pv, acc || kk > 0);
+          mma_ts_w(tbase + C::O_COL(h), tbase + C::S_COL(h) + kk * 8, db, id_pv, acc || kk > 0);
         }
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.err) &&
-                mbar_wait(&k_full[0], 0, abort_flag, a.err);
+      bool ok = warp_wait(q_full, 0, abort_flag, a.err) &&
+                warp_wait(&k_full[0], 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
         qk(0, 0);
-        mma_commit(&s_full[0]);
+        mma_commit_w(&s_full[0]);
         qk(1, 0);
-        mma_commit(&s_full[1]);
-        mma_commit(&k_empty[0]);
+        mma_commit_w(&s_full[1]);
+        mma_commit_w(&k_empty[0]);
         for (int j = 0; j < n && ok; ++j) {
           const int s = j % C::NS;
           const bool more = j + 1 < n;
           const int s1 = (j + 1) % C::NS;
-          if (!mbar_wait(&v_full[s], (j / C::NS) & 1, abort_flag, a.err)) break;
-          if (!mbar_wait(&p_full[0], j & 1, abort_flag, a.err)) break;
+          if (!warp_wait(&v_full[s], (j / C::NS) & 1, abort_flag, a.err)) break;
+          if (!warp_wait(&p_full[0], j & 1, abort_flag, a.err)) break;
           tc_fence_after();
           pv(0, s, j > 0);
           if (more) {
-            if (!mbar_wait(&k_full[s1], ((j + 1) / C::NS) & 1, abort_flag, a.err)) break;
+            if (!warp_wait(&k_full[s1], ((j + 1) / C::NS) & 1, abort_flag, a.err)) break;
             tc_fence_after();
             qk(0, s1);
-            mma_commit(&s_full[0]);
+            mma_commit_w(&s_full[0]);
           }
-          if (!mbar_wait(&p_full[1], j & 1, abort_flag, a.err)) break;
+          if (!warp_wait(&p_full[1], j & 1, abort_flag, a.err)) break;
           tc_fence_after();
           pv(1, s, j > 0);
-          mma_commit(&v_empty[s]);
+          mma_commit_w(&v_empty[s]);
           if (more) {
             qk(1, s1);
-            mma_commit(&s_full[1]);
-            mma_commit(&k_empty[s1]);
+            mma_commit_w(&s_full[1]);
+            mma_commit_w(&k_empty[s1]);
           }
         }
-        mma_commit(o_final);
+        mma_commit_w(o_final);
       }
-      // Every MMA this thread issued must finish before TMEM is released.
-      mma_commit(drain);
+      // Every MMA this warp issued must finish before TMEM is released.
+      mma_commit_w(drain);
       mbar_drain(drain, 0, a.err);
     }
   } else {

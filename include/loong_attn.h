@@ -235,7 +235,7 @@ LOONG_API int loong_attn_bwd(const loong_attn_desc* desc, const void* q, const v
 /*
  * Largest workspace, in bytes, that loong_attn_bwd_noalloc can serve: 32 MiB.
  * A problem fits when loong_attn_workspace_size(desc, 1) is at most this; in
- * FUSED mode that size is at most 4*B*S*Hq*d + 8*B*S*Hkv*d +
+ * FUSED and STEPWISE mode that size is at most 4*B*S*Hq*d + 8*B*S*Hkv*d +
  * 8*B*Hq*(S + 3*nblocks + 128) bytes plus 256 per part (four parts), with
  * nblocks = 2cp (ZIGZAG) or cp.  For example S = 4096 tokens, Hq = 8, Hkv = 1,
  * d = 128 needs about 20.3 MiB.

@@ -94,6 +94,7 @@ def test_workspace_sizes(loong_lib):
     assert ops.loong_attn_workspace_size(copy, 0) == up(kv_el * 2) + 256 + q_el * 4 + 4 * up(kv_el * 2)
     blk = w.seqlen // (2 * w.cp)
     stats = 2 * w.hq * (2 * w.cp * ((blk + 3) // 4 * 4) + 128) * 4
+    # the backward: fp32 dQ accumulator, row statistics, fp32 dK, dV accumulators
     assert ops.loong_attn_workspace_size(fused, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
     assert ops.loong_attn_workspace_size(step, 1) == up(q_el * 4) + up(stats) + 2 * up(kv_el * 4)
     bad = _desc(hq=30)
@@ -233,12 +234,13 @@ def test_headctx_pack_n_validation_before_any_cuda_call(loong_lib):
 
 def test_noalloc_scratch_example_fits(loong_lib):
     """The header's example for the allocation-free backward (S = 4096,
-    Hq = 8, Hkv = 1, d = 128, FUSED) fits its 32 MiB array, within the header's
-    bound."""
+    Hq = 8, Hkv = 1, d = 128) fits its 32 MiB array in FUSED and STEPWISE
+    mode, within the header's bound."""
     w = inputs.Workload("example", 4096, 8, 1, 128, 1, 4, 2, 2, True)
-    need = ops.loong_attn_workspace_size(ops.make_desc(w), 1)
-    assert need <= ops.NOALLOC_SCRATCH_BYTES
-    nblocks = 2 * w.cp
-    estimate = 4 * w.seqlen * w.hq * 128 + 8 * w.seqlen * w.hkv * 128 + 8 * w.hq * (w.seqlen + 3 * nblocks + 128)
-    assert estimate - 8 * w.hq * 3 * nblocks <= need <= estimate + 4 * 256   # block padding, 256-byte rounding
-    assert abs(need / 2 ** 20 - 20.3) < 0.05
+    for mode in (ops.MODE_FUSED, ops.MODE_STEPWISE):
+        need = ops.loong_attn_workspace_size(ops.make_desc(w, mode), 1)
+        assert need <= ops.NOALLOC_SCRATCH_BYTES
+        nblocks = 2 * w.cp
+        estimate = 4 * w.seqlen * w.hq * 128 + 8 * w.seqlen * w.hkv * 128 + 8 * w.hq * (w.seqlen + 3 * nblocks + 128)
+        assert estimate - 8 * w.hq * 3 * nblocks <= need <= estimate + 4 * 256   # block padding, 256-byte rounding
+        assert abs(need / 2 ** 20 - 20.3) < 0.05, need / 2 ** 20
