@@ -55,8 +55,10 @@ struct BwdCfg {
   static constexpr int NBARS = 1 + 4 * NS + 13;
   static constexpr int STAT_BYTES = 2 * kTile * 4;  // LSE*log2e and D of one query tile
   // Tiles first (1024-byte aligned, checked at run time), then the row
-  // statistics stages, the barriers, the TMEM base address and the abort flag.
-  static constexpr int SMEM_BYTES = (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16;
+  // statistics stages, the barriers, the TMEM base address and the abort
+  // flag, then one iteration descriptor per stage.
+  static constexpr int SMEM_BYTES =
+      (2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16 + NS * 16;
   // Compute groups of four warps, each covering all 128 TMEM lanes: group g
   // owns query columns [GW g, GW (g+1)) of S^T / dP^T and head-dim columns
   // [GD g, GD (g+1)) of dQ.  Four groups (four compute warps per scheduler)
@@ -153,6 +155,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint32_t& tmem_base_sh = *reinterpret_cast<uint32_t*>(bars + C::NBARS);
   int& abort_sh = *(reinterpret_cast<int*>(bars + C::NBARS) + 1);
   volatile int* abort_flag = &abort_sh;
+  // Per stage, the iteration the producer loaded into it: view row of the
+  // query tile, its view head, its length, and flags (1: the causal diagonal
+  // tile, 2: a dQ reduction may start there).  Written before the stage's
+  // q_full arrival, so everyone who waited for the stage's data sees it; the
+  // compute and reducer warps then need no walk of their own.
+  int4* sInfo = reinterpret_cast<int4*>(bars + C::NBARS + 2);
 
   // ---- work item: (batch, kv head, key tile); early (heavy) key tiles first
   const RingGeom& g = a.ring;
@@ -218,8 +226,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   if (warp == C::CW) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      mbar_expect_tx(kv_full, 2 * C::TILE_BYTES);
+    {  // the whole warp runs the loop; lane 0 issues
+      const uint32_t leader = lane == 0;
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err));
+      };
+
+      mbar_expect_tx_p(leader, kv_full, 2 * C::TILE_BYTES);
       int kvc;
       // the rank that holds this key tile's chunk at the launch's (single) step
       const int holder = ring_dst(block_owner(g, bk), a.t_begin, g.inner, g.outer);
@@ -229,8 +242,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       in_bounds(kr64 >= 0 && kr64 < a.lay.view_rows(a.batch) && kvc >= 0 && kvc < a.lay.view_heads(a.hkv), a.err);
       const int kr = static_cast<int>(kr64);
       for (int at = 0; at < C::ATOMS; ++at) {
-        tma_load_3d(sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvc, kr);
-        tma_load_3d(sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvc, kr);
+        tma_load_3d_p(leader, sK + at * C::ATOM_BYTES, &tmK, kv_full, at * 64, kvc, kr);
+        tma_load_3d_p(leader, sV + at * C::ATOM_BYTES, &tmV, kv_full, at * 64, kvc, kr);
       }
       int issued = 0;
       for (int i = 0; i < n; ++i, walk.advance()) {
@@ -242,11 +255,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int64_t qrow64 = a.lay.view_row(b, walk.q0(), head, a.hq, hc);
         in_bounds(qrow64 >= 0 && qrow64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
         const int qrow = static_cast<int>(qrow64);
-        if (i >= C::NS && !mbar_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
-        mbar_expect_tx(&q_full[s], 2 * C::TILE_BYTES + C::STAT_BYTES);
+        // checked build: a reduction never starts outside the accumulator (skipped if it would)
+        const bool red_ok =
+            in_bounds(qrow64 >= 0 && qrow64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
+        if (i >= C::NS && !warp_wait(&q_empty[s], (u - 1) & 1, abort_flag, a.err)) break;
+        if (leader) sInfo[s] = make_int4(qrow, hc, walk.qlen(), (walk.diag() ? 1 : 0) | (red_ok ? 2 : 0));
+        mbar_expect_tx_p(leader, &q_full[s], 2 * C::TILE_BYTES + C::STAT_BYTES);
         for (int at = 0; at < C::ATOMS; ++at) {
-          tma_load_3d(sQ + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, &q_full[s], at * 64, hc, qrow);
-          tma_load_3d(sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, hc, qrow);
+          tma_load_3d_p(leader, sQ + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmQ, &q_full[s], at * 64, hc, qrow);
+          tma_load_3d_p(leader, sdO + s * C::TILE_BYTES + at * C::ATOM_BYTES, &tmO, &q_full[s], at * 64, hc, qrow);
         }
         // this tile's row statistics: 16-byte aligned and in bounds by construction
         int64_t srow = (static_cast<int64_t>(b) * a.hq + head) * a.stat_len + walk.bq * a.blk_pad +
@@ -257,8 +274,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                            srow + kTile <= (static_cast<int64_t>(b) * a.hq + head + 1) * a.stat_len,
                        a.err))
           srow = 0;
-        bulk_load(sStat + s * (2 * kTile), a.lse2 + srow, kTile * 4, &q_full[s]);
-        bulk_load(sStat + s * (2 * kTile) + kTile, a.dstat + srow, kTile * 4, &q_full[s]);
+        bulk_load_p(leader, sStat + s * (2 * kTile), a.lse2 + srow, kTile * 4, &q_full[s]);
+        bulk_load_p(leader, sStat + s * (2 * kTile) + kTile, a.dstat + srow, kTile * 4, &q_full[s]);
         ++issued;
       }
       mbar_drain(kv_full, 0, a.err);
@@ -355,39 +372,43 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ dQ reducer
     // Adds each staged dQ tile into the fp32 accumulator with TMA bulk tensor
     // reductions and hands the stage back to the producer once it is read.
-    if (lane == 0) {
-      for (int i = 0; i < n; ++i, walk.advance()) {
+    {  // the whole warp runs the loop; lane 0 issues
+      const uint32_t leader = lane == 0;
+      auto warp_wait = [&](uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err));
+      };
+
+      for (int i = 0; i < n; ++i) {
         const int s = i % C::NS;
-        const int head = kvh * a.G + walk.head;
-        int hc;
-        const int64_t qrow64 = a.lay.view_row(b, walk.q0(), head, a.hq, hc);
-        // checked build: a reduction never starts outside the accumulator (skipped if it would)
-        const bool red_ok =
-            in_bounds(qrow64 >= 0 && qrow64 < a.lay.view_rows(a.batch) && hc >= 0 && hc < a.lay.view_heads(a.hq), a.err);
-        const int qrow = static_cast<int>(qrow64);
         if constexpr (C::EARLY_O) {
           // the dO half first: it is staged without waiting for dK(i)
-          if (!mbar_wait(&staged_o[s], (i / C::NS) & 1, abort_flag, a.err)) break;
+          if (!warp_wait(&staged_o[s], (i / C::NS) & 1, abort_flag, a.err)) break;
+          const int4 info = sInfo[s];  // the producer wrote it before the stage's data
+          const int qrow = info.x, hc = info.y;
+          const bool red_ok = info.w & 2;
 #pragma unroll
           for (int box = C::BOXES_PER_STAGE; box < C::DQ_BOXES; ++box)
             if (red_ok)
-              tma_reduce_add_3d(&tmDQ, sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES,
+              tma_reduce_add_3d_p(leader, &tmDQ, sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES,
                                 box * 32, hc, qrow);
         }
-        if (!mbar_wait(&staged_q[s], (i / C::NS) & 1, abort_flag, a.err)) break;
+        if (!warp_wait(&staged_q[s], (i / C::NS) & 1, abort_flag, a.err)) break;
+        const int4 info = sInfo[s];
+        const int qrow = info.x, hc = info.y;
+        const bool red_ok = info.w & 2;
 #pragma unroll
         for (int box = 0; box < (C::EARLY_O ? C::BOXES_PER_STAGE : C::DQ_BOXES); ++box) {
           const uint8_t* base = box < C::BOXES_PER_STAGE
                                     ? sQ + s * C::TILE_BYTES + box * C::BOX_BYTES
                                     : sdO + s * C::TILE_BYTES + (box - C::BOXES_PER_STAGE) * C::BOX_BYTES;
-          if (red_ok) tma_reduce_add_3d(&tmDQ, base, box * 32, hc, qrow);
+          if (red_ok) tma_reduce_add_3d_p(leader, &tmDQ, base, box * 32, hc, qrow);
         }
-        bulk_commit_group();
-        bulk_wait_read_all();
-        mbar_arrive(&q_empty[s]);
+        bulk_commit_group_p(leader);
+        bulk_wait_read_all_p(leader);
+        mbar_arrive_p(leader, &q_empty[s]);
       }
       // the reductions must land before the kernel ends
-      bulk_wait_all();
+      bulk_wait_all_p(leader);
     }
   } else {
     // ------------------------------------------------------------ compute warps
@@ -411,11 +432,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, a.err));
     };
-    for (int i = 0; i < n; ++i, walk.advance()) {
-      const int head = kvh * a.G + walk.head;
-      const int q0 = walk.q0();
-      const int qlen = walk.qlen();
-      const bool dg = walk.diag();
+    for (int i = 0; i < n; ++i) {
       // row statistics of this tile, staged by the producer with Q and dO
       const float* lse_row = sStat + (i % C::NS) * (2 * kTile);
       const float* d_row = lse_row + kTile;
@@ -425,6 +442,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         break;
       }
       tc_fence_after();
+      // S^T(i) read Q(i): the stage's descriptor is in place
+      const int4 info = sInfo[i % C::NS];
+      const int qlen = info.z;
+      const bool dg = info.w & 1;
       float pv[C::GCH][32];
       {
         uint32_t sv[C::GCH][32];
@@ -484,7 +505,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      mbar_arrive_p(lane == 0, p_full);
 
       // ---- dS^T = P^T * (dP^T - D) into shared memory
       if (!warp_wait(dp_full, i & 1)) {
@@ -534,7 +555,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      mbar_arrive_p(lane == 0, ds_full);
 
       // ---- drain dQ (queries on lanes): TMEM -> registers, R1 released, then
       // staged (fp32, 128-byte swizzled boxes of 32 columns) into this
@@ -561,7 +582,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(dq_empty);
+        mbar_arrive_p(lane == 0, dq_empty);
         // groups staging into the Q half wait for dK(i), which may still read
         // it; the others write the dO half, whose last reader dV(i) retired
         // before dQ(i)
@@ -591,7 +612,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(q_half ? &staged_q[s] : &staged_o[s]);
+        mbar_arrive_p(lane == 0, q_half ? &staged_q[s] : &staged_o[s]);
       }
 
       // ---- every kFlush iterations: fold dV / dK into the fp32 accumulators
@@ -621,7 +642,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty);
+        mbar_arrive_p(lane == 0, acc_empty);
       }
     }
     // ---------------------------------------------------------- epilogue

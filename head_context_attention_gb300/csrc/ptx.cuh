@@ -168,6 +168,66 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The copy and barrier operations above for a warp whose 32 lanes all run the
+// loop (warp-uniform control flow): the lane with `leader` != 0 acts, the
+// others skip the instruction without branching.
+__device__ __forceinline__ void mbar_expect_tx_p(uint32_t leader, uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"(leader),
+      "r"(smem_u32(bar)), "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_p(uint32_t leader, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%1];\n\t}" ::"r"(leader),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_p(uint32_t leader, void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int c0, int c1, int c2) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%1], [%2, {%4, %5, %6}], [%3];\n\t}" ::"r"(leader),
+      "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load_p(uint32_t leader, void* dst, const void* src, uint32_t bytes,
+                                            uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%1], [%2], %3, [%4];\n\t}" ::"r"(
+          leader),
+      "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d_p(uint32_t leader, const CUtensorMap* map, const void* src, int c0,
+                                                    int c1, int c2) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(leader),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group_p(uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p cp.async.bulk.commit_group;\n\t}" ::"r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all_p(uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p cp.async.bulk.wait_group.read 0;\n\t}" ::"r"(leader)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all_p(uint32_t leader) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p cp.async.bulk.wait_group 0;\n\t}" ::"r"(leader)
+      : "memory");
+}
+
 // ------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
