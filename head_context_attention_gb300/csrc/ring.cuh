@@ -148,8 +148,15 @@ struct KvWalk {
     return e < kTile ? e : kTile;
   }
   __host__ __device__ bool diag() const { return g.causal && bk == bq && kt == qi; }
+  // The next tile: within the block without recomputing the ring position
+  // (the ring arithmetic divides by the ring sizes), else the next block.
   __host__ __device__ void advance() {
-    ++kt;
+    if (++kt < kt_n) return;
+    kt = 0;
+    if (++part == rank_parts(g)) {
+      part = 0;
+      ++t;
+    }
     settle();
   }
   // Number of tiles left, walking a copy.
@@ -190,6 +197,7 @@ struct QWalk {
   RingGeom g;
   int G, bk, kt, j, t, t1, part, rot;
   int qlo, len, k, hk;  // tiles [qlo, ntile) of the current block; position k; head position hk
+  int rot_len, rot_g;   // rot reduced modulo len (per block) and modulo G
   int qi, head, bq;
 
   __host__ __device__ void init(const RingGeom& geom, int G_, int bk_, int kt_, int t0, int t1_, int rot_ = 0) {
@@ -202,6 +210,7 @@ struct QWalk {
     t1 = t1_;
     part = 0;
     rot = rot_ < 0 ? 0 : rot_;
+    rot_g = rot % G;
     next_block(true);
   }
   // Settle on the first (tile, head) of the current or next block that sees bk.
@@ -215,6 +224,7 @@ struct QWalk {
       if (len > 0) {
         k = 0;
         hk = 0;
+        rot_len = rot % len;
         set();
         return;
       }
@@ -227,9 +237,13 @@ struct QWalk {
       ++t;
     }
   }
+  // qi = qlo + (k + rot) mod len, head = (hk + rot) mod G, without dividing
+  // (k < len, hk < G)
   __host__ __device__ void set() {
-    qi = qlo + (k + rot) % len;
-    head = (hk + rot) % G;
+    const int x = k + rot_len;
+    qi = qlo + (x >= len ? x - len : x);
+    const int y = hk + rot_g;
+    head = y >= G ? y - G : y;
   }
   __host__ __device__ bool done() const { return t >= t1; }
   __host__ __device__ void advance() {
