@@ -88,6 +88,9 @@ struct BwdCfg {
   static constexpr bool EARLY_O = true;
   // groups whose dQ columns lie in the Q half of the stage (the rest: the dO half)
   static constexpr int QHALF_GROUPS = BOXES_PER_STAGE * 32 / GD;
+  // the iteration descriptors (int4) after the barriers and two words
+  static_assert(((2 + 2 * NS) * TILE_BYTES + DS_BYTES + NS * STAT_BYTES + NBARS * 8 + 16) % 16 == 0,
+                "descriptor alignment");
 };
 
 // dK and dV build up in tensor memory; every kFlush iterations they are added
