@@ -29,10 +29,16 @@
 // Warp roles (320 threads): warps 0-3 softmax for head slot 0, warps 4-7 for
 // head slot 1 (warp w reads TMEM lanes 32*(w%4)..+31, the rows it owns),
 // warp 8 issues TMA loads, warp 9 allocates TMEM and issues the MMAs.
-// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
-// that (d columns each).  P_h overwrites the first 64 columns of S_h as fp16
-// pairs; the next Q K^T into S_h is issued after O_h += P_h V and tcgen05
-// operations issued by one thread execute in order.
+// Tensor memory (512 columns): NSB score buffers of 128 columns, then O_0 and
+// O_1 (d columns each).  The MMA jobs (key tile j, head h) run in the order
+// J = 2j + h and job J's scores go to buffer J mod NSB; P overwrites the first
+// 64 columns of its buffer as fp16 pairs.  Job J's Q K^T is issued right after
+// job J - NSB's P V (tcgen05 operations issued by one thread execute in
+// order, so the buffer is free by then).  With NSB = 2 (d = 128, where O
+// takes the rest of tensor memory) a head's next scores wait for its own P V;
+// with NSB = 3 (d = 64) they are computed while the softmax still works on the
+// current tile, and a softmax that rescales O_h first waits for the previous
+// P V into O_h.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -52,12 +58,14 @@ struct FwdCfg {
   static constexpr int ATOMS = D / 64;             // 128-byte swizzle atoms per row
   static constexpr int ATOM_BYTES = kTile * 128;   // one atom column of a tile
   static constexpr int TILE_BYTES = kTile * D * 2;
-  static constexpr int NBARS = 1 + 4 * NS + 2 + 2 + 2;
+  static constexpr int NSB = D == 64 ? 3 : 2;      // score buffers in tensor memory
+  static constexpr int NBARS = 1 + 4 * NS + 3 + 3 + 2 + 2;
   static constexpr int SMEM_BYTES = (NQ + 2 * NS) * TILE_BYTES + NBARS * 8 + 1024;
   static constexpr int THREADS = 320;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t S_COL(int h) { return static_cast<uint32_t>(h) * 128u; }
-  static constexpr uint32_t O_COL(int h) { return 256u + static_cast<uint32_t>(h) * D; }
+  __host__ __device__ static constexpr uint32_t S_COL(int buf) { return static_cast<uint32_t>(buf) * 128u; }
+  __host__ __device__ static constexpr uint32_t O_COL(int h) { return NSB * 128u + static_cast<uint32_t>(h) * D; }
+  static_assert(NSB * 128 + 2 * D <= 512, "tensor memory");
 };
 
 struct FwdArgs {
@@ -103,9 +111,14 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* k_empty = k_full + C::NS;
   uint64_t* v_full = k_empty + C::NS;
   uint64_t* v_empty = v_full + C::NS;
-  uint64_t* s_full = v_empty + C::NS;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_final = p_full + 2;
+  uint64_t* s_full = v_empty + C::NS;  // NSB: scores in the buffer (MMA -> softmax of its head)
+  // NSB: P of the buffer's job stored (softmax -> MMA).  Per buffer, not per
+  // head: a head's softmax may finish two tiles before the MMA warp takes the
+  // first P, but a buffer's next P needs that buffer's next scores, issued
+  // only after the MMA warp has taken this one.
+  uint64_t* p_full = s_full + 3;
+  uint64_t* pv_done = p_full + 3;      // 2: O_h += P V done (MMA -> softmax, before a rescale)
+  uint64_t* o_final = pv_done + 2;
   uint64_t* drain = o_final + 1;
   volatile int* abort_flag = &abort_sh;
 
@@ -148,10 +161,11 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&s_full[h], 1);
-      mbar_init(&p_full[h], 4);
+    for (int sb = 0; sb < C::NSB; ++sb) {
+      mbar_init(&s_full[sb], 1);
+      mbar_init(&p_full[sb], 4);
     }
+    for (int h = 0; h < 2; ++h) mbar_init(&pv_done[h], 1);
     mbar_init(o_final, 1);
     mbar_init(drain, 1);
     abort_sh = 0;
@@ -223,53 +237,57 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_f16(128, D, false, true);  // P and V in fp16
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      auto qk = [&](int h, int s) {
+      auto qk = [&](int h, int s, int buf) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
           const uint64_t da = sdesc_sw128(q_addr + h * C::TILE_BYTES + off, 16, 1024);
           const uint64_t db = sdesc_sw128(k_addr + s * C::TILE_BYTES + off, 16, 1024);
-          mma_ss_w(tbase + C::S_COL(h), da, db, id_qk, kk > 0);
+          mma_ss_w(tbase + C::S_COL(buf), da, db, id_qk, kk > 0);
         }
       };
-      auto pv = [&](int h, int s, bool acc) {
+      auto pv = [&](int h, int s, int buf, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t db = sdesc_sw128(v_addr + s * C::TILE_BYTES + kk * 2048, C::ATOM_BYTES, 1024);
-          mma_ts_w(tbase + C::O_COL(h), tbase + C::S_COL(h) + kk * 8, db, id_pv, acc || kk > 0);
+          mma_ts_w(tbase + C::O_COL(h), tbase + C::S_COL(buf) + kk * 8, db, id_pv, acc || kk > 0);
         }
       };
-      bool ok = warp_wait(q_full, 0, abort_flag, a.err) &&
-                warp_wait(&k_full[0], 0, abort_flag, a.err);
+      // Q K^T of job J = 2 jt + h into buffer J mod NSB; K(jt) is released
+      // after its second head
+      auto issue_qk = [&](int J) {
+        const int jt = J >> 1, h = J & 1, st = jt % C::NS;
+        if (h == 0) {
+          if (!warp_wait(&k_full[st], (jt / C::NS) & 1, abort_flag, a.err)) return false;
+          tc_fence_after();
+        }
+        qk(h, st, J % C::NSB);
+        mma_commit_w(&s_full[J % C::NSB]);
+        if (h == 1) mma_commit_w(&k_empty[st]);
+        return true;
+      };
+      bool ok = warp_wait(q_full, 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
-        qk(0, 0);
-        mma_commit_w(&s_full[0]);
-        qk(1, 0);
-        mma_commit_w(&s_full[1]);
-        mma_commit_w(&k_empty[0]);
+        for (int J = 0; J < C::NSB && J < 2 * n && ok; ++J) ok = issue_qk(J);
         for (int j = 0; j < n && ok; ++j) {
           const int s = j % C::NS;
-          const bool more = j + 1 < n;
-          const int s1 = (j + 1) % C::NS;
           if (!warp_wait(&v_full[s], (j / C::NS) & 1, abort_flag, a.err)) break;
-          if (!warp_wait(&p_full[0], j & 1, abort_flag, a.err)) break;
-          tc_fence_after();
-          pv(0, s, j > 0);
-          if (more) {
-            if (!warp_wait(&k_full[s1], ((j + 1) / C::NS) & 1, abort_flag, a.err)) break;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int J = 2 * j + h;
+            if (!warp_wait(&p_full[J % C::NSB], (J / C::NSB) & 1, abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            qk(0, s1);
-            mma_commit_w(&s_full[0]);
-          }
-          if (!warp_wait(&p_full[1], j & 1, abort_flag, a.err)) break;
-          tc_fence_after();
-          pv(1, s, j > 0);
-          mma_commit_w(&v_empty[s]);
-          if (more) {
-            qk(1, s1);
-            mma_commit_w(&s_full[1]);
-            mma_commit_w(&k_empty[s1]);
+            pv(h, s, J % C::NSB, j > 0);
+            mma_commit_w(&pv_done[h]);
+            if (h == 1) mma_commit_w(&v_empty[s]);
+            if (J + C::NSB < 2 * n && !issue_qk(J + C::NSB)) {
+              ok = false;
+              break;
+            }
           }
         }
         mma_commit_w(o_final);
@@ -284,7 +302,6 @@ __global__ void __launch_bounds__(320, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tbase + t_lane + C::S_COL(h);
     const uint32_t tO = tbase + t_lane + C::O_COL(h);
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;
@@ -292,7 +309,9 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int j = 0; j < n; ++j, walk.advance()) {
       // Lanes leave together so the .sync.aligned TMEM accesses never diverge.
-      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[h], j & 1, abort_flag, a.err))) {
+      const int J = 2 * j + h;  // this tile's MMA job and its score buffer
+      const uint32_t tS = tbase + t_lane + C::S_COL(J % C::NSB);
+      if (!__all_sync(0xffffffffu, mbar_wait(&s_full[J % C::NSB], (J / C::NSB) & 1, abort_flag, a.err))) {
         ok = false;
         break;
       }
@@ -327,7 +346,14 @@ __global__ void __launch_bounds__(320, 1)
       // The decision is per row, but TMEM loads and stores are warp-collective:
       // the whole warp takes the branch, rows that need none scale by 1.
       if (__any_sync(0xffffffffu, rescale)) {
-        // O_h is stable: the commit that signalled S_h follows O_h += P V.
+        // O_h must hold the previous tile's P V: with two buffers the commit
+        // that signalled these scores follows it; with three, wait for it
+        // (completion j - 1 of pv_done[h]; completion j needs this tile's P)
+        if (C::NSB > 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[h], (j - 1) & 1, abort_flag, a.err))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         const float f = rescale ? fast_exp2(m_run - m_new) : 1.f;
         l_run *= f;
 #pragma unroll 1
@@ -365,7 +391,7 @@ __global__ void __launch_bounds__(320, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[h]);
+      if (lane == 0) mbar_arrive(&p_full[J % C::NSB]);
     }
     // ---------------------------------------------------------- epilogue
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, abort_flag, a.err));
