@@ -80,7 +80,14 @@ def test_recorded_traffic_follows_kernel_sources(monkeypatch):
     was taken on; any other source hash gives null traffic."""
     rec = json.load(open(os.path.join(ROOT, "profiles", "roofline_traffic.json")))
     ent = rec["kernels"]["ring_bwd_kernel"]["llama3-8b-s128k"]["rank-major"]
-    assert ent["dram_bytes_per_launch"] == ent["dram_read_bytes"] + ent["dram_write_bytes"]
+    # the small-case capture scaled by tile iterations: Hkv * G * nt(nt+1)/2, nt = S/128
+    from head_context_attention_gb300 import inputs
+    w = inputs.WORKLOADS["llama3-8b-s128k"]
+    tiles = lambda S: w.hkv * (w.hq // w.hkv) * (S // 128) * (S // 128 + 1) // 2
+    small = ent["measured_s16384"]
+    assert small["tile_iterations"] == tiles(16384)
+    want = (small["dram_read_bytes"] + small["dram_write_bytes"]) * tiles(w.seqlen) / tiles(16384)
+    assert ent["dram_bytes_per_launch"] == round(want)
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha256"])
     assert bench.recorded_traffic("ring_bwd_kernel", "llama3-8b-s128k") == ent["dram_bytes_per_launch"]
     assert bench.recorded_traffic("ring_bwd_kernel", "no-such-workload") is None
