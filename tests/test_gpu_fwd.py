@@ -54,6 +54,23 @@ def test_forward_matches_oracle(cuda_device, name, mode):
     assert_close("LSE", to64(lse), want_lse, LSE_ATOL, 0.0)
 
 
+@pytest.mark.parametrize("mode", [ops.MODE_FUSED, ops.MODE_STEPWISE])
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_with_peaky_keys_matches_oracle(cuda_device, d, mode):
+    """Keys scaled x8 at 5 % of the positions make a row's running maximum jump
+    by more than the lazy-rescale threshold at many tiles of a long walk (16
+    paired blocks, 32 key tiles for the last query tile), so O is rescaled
+    often.  At d = 64 the scores of a head's next tile are computed while its
+    previous P V may still be queued; each rescale first waits for that P V."""
+    w = inputs.Workload("peaky-fwd", 4096, 4, 2, d, 2, 8, 4, 2, False, placement=1, peaky_keys=0.05)
+    x = inputs.make_inputs(w, device="cuda", with_do=False)
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"], mode=mode)
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    want_o, want_lse = _oracle(w, x)
+    assert_close("O", to64(o), want_o, O_ATOL, O_RTOL)
+    assert_close("LSE", to64(lse), want_lse, LSE_ATOL, 0.0)
+
+
 def test_chunked_oracle_agrees_on_gpu_inputs(cuda_device):
     """The GPU result also matches the second (ring-walking) oracle."""
     w = _workload("d128-double-ring")
