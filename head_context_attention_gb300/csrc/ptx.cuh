@@ -133,44 +133,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// Contiguous global -> shared copy of `bytes` (multiple of 16, both addresses
-// 16-byte aligned), completing on `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Element-wise add of a shared-memory box into global memory (tensor map),
-// tracked by the issuing thread's bulk async-group.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int c0, int c1,
-                                                  int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until the shared memory read by this thread's bulk groups may be reused.
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// Wait until this thread's bulk groups have fully completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// The copy and barrier operations above for a warp whose 32 lanes all run the
-// loop (warp-uniform control flow): the lane with `leader` != 0 acts, the
-// others skip the instruction without branching.
+// Copy and barrier operations for a warp whose 32 lanes all run the loop
+// (warp-uniform control flow): the lane with `leader` != 0 acts, the others
+// skip the instruction without branching.
 __device__ __forceinline__ void mbar_expect_tx_p(uint32_t leader, uint64_t* bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
@@ -194,6 +163,8 @@ __device__ __forceinline__ void tma_load_3d_p(uint32_t leader, void* dst, const 
       "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// Contiguous global -> shared copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), completing on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load_p(uint32_t leader, void* dst, const void* src, uint32_t bytes,
                                             uint64_t* bar) {
   asm volatile(
@@ -203,6 +174,8 @@ __device__ __forceinline__ void bulk_load_p(uint32_t leader, void* dst, const vo
       "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Element-wise add of a shared-memory box into global memory (tensor map),
+// tracked by the issuing lane's bulk async-group.
 __device__ __forceinline__ void tma_reduce_add_3d_p(uint32_t leader, const CUtensorMap* map, const void* src, int c0,
                                                     int c1, int c2) {
   asm volatile(
@@ -217,11 +190,13 @@ __device__ __forceinline__ void bulk_commit_group_p(uint32_t leader) {
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p cp.async.bulk.commit_group;\n\t}" ::"r"(leader)
       : "memory");
 }
+// Wait until the shared memory read by the lane's bulk groups may be reused.
 __device__ __forceinline__ void bulk_wait_read_all_p(uint32_t leader) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p cp.async.bulk.wait_group.read 0;\n\t}" ::"r"(leader)
       : "memory");
 }
+// Wait until the lane's bulk groups have fully completed.
 __device__ __forceinline__ void bulk_wait_all_p(uint32_t leader) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p cp.async.bulk.wait_group 0;\n\t}" ::"r"(leader)
@@ -249,38 +224,12 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 operation issued so far by this
-// thread has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-
-// The same three operations for an MMA warp whose 32 lanes all run the issue
-// loop (warp-uniform control flow, every lane of the warp calls them): one
-// lane chosen by elect.sync issues.  A lone issuing lane inside a divergent
+// MMAs and their commit, for an MMA warp whose 32 lanes all run the issue loop
+// (warp-uniform control flow, every lane of the warp calls them): one lane
+// chosen by elect.sync issues.  mma_ss_w: D[tmem] (+)= A[smem] * B[smem];
+// mma_ts_w: D[tmem] (+)= A[tmem] * B[smem]; mma_commit_w: arrive once on the
+// barrier when every tcgen05 operation the lane issued so far has completed
+// (the same lane is elected every time).  A lone issuing lane inside a divergent
 // branch pays for every further branch with an idle tensor pipe (measured:
 // about 60 cycles per branch between MMAs); with the whole warp in the loop a
 // wait between MMA groups costs nothing measurable.
@@ -351,24 +300,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-
-// 32 lanes x 8 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
       : "memory");
 }
 
