@@ -723,17 +723,20 @@ def run_gpu(args, w, rank, local, world, pg):
 
 
 def pinned_buffers(w, path, x):
-    """Pinned host copies of the inputs and pinned host buffers for the outputs."""
-    import torch
+    """Pinned host copies of the inputs and pinned host buffers for the outputs,
+    from the library's host allocator (loong_host_alloc: registered memory on
+    transparent huge pages, which keeps the copies at full speed when the
+    device's translations of host pages have gone cold)."""
+    from head_context_attention_gb300 import ops
 
     names = path.FWD_IN + (path.BWD_IN if w.backward else ())
-    host_in = {n: torch.empty(x[n].shape, dtype=x[n].dtype, pin_memory=True) for n in names}
+    host_in = {n: ops.host_empty(x[n].shape, x[n].dtype) for n in names}
     for n in names:
         host_in[n].copy_(x[n])
     outs = dict(path.out, lse=path.lse)
     if not w.backward:
         outs = {"o": path.out["o"], "lse": path.lse}
-    host_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+    host_out = {n: ops.host_empty(t.shape, t.dtype) for n, t in outs.items()}
     return host_in, host_out
 
 
@@ -822,7 +825,7 @@ def run_e2e(args, w, path, dev, stream, world, pg, x, bufs):
         raise SystemExit("device status after the end-to-end leg")
     return {"value": round(w.flops * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "api": "loong_attn_2d_host (C ABI, pinned host buffers)",
+            "api": "loong_attn_2d_host (C ABI, host buffers from loong_host_alloc)",
             "copies": ("library copy streams overlapped with the kernels, two input slots" if overlap
                        else "in series: each call synchronised before the next"),
             "copy_alone_ms": copy_ms}

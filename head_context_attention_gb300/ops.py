@@ -32,7 +32,7 @@ EXPORTS = ("loong_version", "loong_status_string", "loong_last_cuda_error", "loo
            "loong_attn_workspace_size", "loong_ring_schedule", "loong_attn_fwd", "loong_attn_fwd_ranks",
            "loong_attn_bwd",
            "loong_attn_bwd_noalloc", "loong_lse_merge", "loong_headctx_pack", "loong_headctx_pack_n",
-           "loong_attn_2d_host_workspace_size", "loong_attn_2d_host",
+           "loong_attn_2d_host_workspace_size", "loong_attn_2d_host", "loong_host_alloc", "loong_host_free",
            "loong_set_timing_events", "loong_get_device_status", "loong_selftest_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 32 << 20   # LOONG_NOALLOC_SCRATCH_BYTES
 
@@ -88,6 +88,8 @@ def lib():
         L.loong_attn_2d_host_workspace_size.restype = SZ
         L.loong_attn_2d_host_workspace_size.argtypes = [D, ctypes.c_int]
         L.loong_attn_2d_host.argtypes = [D, I32, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+        L.loong_host_alloc.argtypes = [SZ, ctypes.POINTER(ctypes.c_void_p)]
+        L.loong_host_free.argtypes = [P]
         L.loong_set_timing_events.argtypes = [P, P]
         L.loong_get_device_status.argtypes = [P]
         L.loong_selftest_wait_timeout.argtypes = [ctypes.c_uint32, P]
@@ -197,6 +199,44 @@ def loong_attn_2d_host(desc, slot, q, k, v, dout, o, lse, dq, dk, dv, ws, stream
     return _check("loong_attn_2d_host", lib().loong_attn_2d_host(
         ctypes.byref(desc), slot, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(o), _ptr(lse), _ptr(dq),
         _ptr(dk), _ptr(dv), _ptr(ws), nbytes, _stream(stream), ev))
+
+
+def loong_host_alloc(nbytes):
+    """Pinned, huge-page-backed host memory of ``nbytes`` bytes (an address,
+    or None for 0 bytes); release it with loong_host_free."""
+    p = ctypes.c_void_p()
+    _check("loong_host_alloc", lib().loong_host_alloc(nbytes, ctypes.byref(p)))
+    return p.value
+
+
+def loong_host_free(ptr):
+    return _check("loong_host_free", lib().loong_host_free(ptr))
+
+
+_HOST_BUFFERS = {}
+
+
+def host_empty(shape, dtype):
+    """A CPU tensor over loong_host_alloc memory (pinned, huge pages where the
+    kernel offers them), for the host arguments of loong_attn_2d_host.  It
+    stays allocated until host_release(t) or the end of the process."""
+    n = 1
+    for e in shape:
+        n *= int(e)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    if nbytes == 0:
+        return torch.empty(shape, dtype=dtype)
+    ptr = loong_host_alloc(nbytes)
+    raw = (ctypes.c_uint8 * nbytes).from_address(ptr)
+    t = torch.frombuffer(raw, dtype=torch.uint8).view(dtype).view(shape)
+    _HOST_BUFFERS[t.data_ptr()] = (ptr, raw)
+    return t
+
+
+def host_release(t):
+    """Free the memory of a host_empty tensor; the tensor must not be used afterwards."""
+    ptr, _ = _HOST_BUFFERS.pop(t.data_ptr())
+    loong_host_free(ptr)
 
 
 def loong_set_timing_events(start=None, stop=None):

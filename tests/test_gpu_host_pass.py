@@ -142,6 +142,40 @@ def test_pageable_host_memory_works(cuda_device):
     _check_equal(w, hout, _device_pass(w, x, ops.LAYOUT_RANK_MAJOR))
 
 
+def test_library_host_buffers_work_and_are_pinned(cuda_device):
+    """Inputs and outputs in loong_host_alloc memory (registered, on huge pages
+    where the kernel offers them): torch sees it as pinned, the pass equals the
+    device path, and every buffer is released again."""
+    w = inputs.small(2048, 8, 2, 128, hp=2, cp=4, inner=2, outer=2)
+    x = inputs.make_inputs(w, device="cuda")
+    desc = ops.make_desc(w, layout=ops.LAYOUT_RANK_MAJOR)
+    ws = torch.empty(ops.loong_attn_2d_host_workspace_size(desc, 1), dtype=torch.uint8, device="cuda")
+    hin = {n: ops.host_empty(t.shape, t.dtype) for n, t in x.items()}
+    for n, t in x.items():
+        hin[n].copy_(t)
+    _, ref_out = _host_buffers(w, x)
+    hout = {n: ops.host_empty(t.shape, t.dtype) for n, t in ref_out.items()}
+    assert all(t.is_pinned() for t in list(hin.values()) + list(hout.values()))
+    _host_pass(desc, w, 0, hin, hout, ws)
+    torch.cuda.synchronize()
+    _check_equal(w, hout, _device_pass(w, x, ops.LAYOUT_RANK_MAJOR))
+    for t in list(hin.values()) + list(hout.values()):
+        ops.host_release(t)
+
+
+def test_host_allocator_edge_cases(cuda_device):
+    """Zero bytes gives no buffer; freeing NULL is a no-op; a pointer the
+    allocator did not return is refused."""
+    assert ops.loong_host_alloc(0) is None
+    assert ops.lib().loong_host_free(None) == ops.LOONG_OK
+    foreign = torch.empty(16, dtype=torch.uint8, pin_memory=True)
+    assert ops.lib().loong_host_free(foreign.data_ptr()) == ops.LOONG_ERR_INVALID_ARG
+    p = ops.loong_host_alloc(1)
+    assert p is not None
+    assert ops.lib().loong_host_free(p) == ops.LOONG_OK
+    assert ops.lib().loong_host_free(p) == ops.LOONG_ERR_INVALID_ARG
+
+
 def test_device_memory_in_host_arguments_is_refused(cuda_device):
     w = inputs.small(1024, 4, 2, 64, hp=2, cp=2, inner=2)
     x = inputs.make_inputs(w, device="cuda")
