@@ -357,8 +357,10 @@ LOONG_API size_t loong_attn_2d_host_workspace_size(const loong_attn_desc* desc, 
  * call's input copies start when the call is made, once the slot's previous
  * inputs have been read; dO arrives while the forward runs, and O and LSE
  * leave while the backward runs.  Pinned host memory (cudaHostAlloc /
- * cudaHostRegister) lets the copies overlap the kernels; pageable memory is
- * accepted but copies synchronously.  The caller must not change the inputs
+ * cudaHostRegister, or loong_host_alloc below, which also keeps the copies at
+ * full speed when the device's translations of host pages have gone cold)
+ * lets the copies overlap the kernels; pageable memory is accepted but
+ * copies synchronously.  The caller must not change the inputs
  * or read the outputs before the call's work has finished (done_event, or
  * `stream` when done_event is NULL).  Calls on one device are serialised by
  * the library (one enqueue at a time).  Device pointers in the host
