@@ -298,26 +298,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       constexpr uint32_t id_dq = idesc_bf16(128, D, true, true);     // dQ: A and B MN-major
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ),
                      o_addr = smem_u32(sdO), ds_addr = smem_u32(sdS);
+      // Descriptors built once: an operand's descriptor at byte offset `off`
+      // is its base descriptor plus off / 16 (the 14-bit address field cannot
+      // carry: every shared-memory address is below 256 KB).
+      auto d16 = [](uint32_t a) { return sdesc_sw128(a, 16, 1024); };           // K-major operands
+      auto dmn = [](uint32_t a) { return sdesc_sw128(a, C::ATOM_BYTES, 1024); };  // MN-major operands
+      const uint64_t k16 = d16(k_addr), kmn = dmn(k_addr), v16 = d16(v_addr), ds16 = d16(ds_addr),
+                     dsmn = dmn(ds_addr);
       // X^T[keys x queries] = A[keys x d] * B[queries x d]^T, both K-major
-      auto mm_s = [&](uint32_t dst, uint32_t a_base, uint32_t b_base) {
+      auto mm_s = [&](uint32_t dst, uint64_t a_desc, uint64_t b_desc) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
-          mma_ss_w(tbase + dst, sdesc_sw128(a_base + off, 16, 1024), sdesc_sw128(b_base + off, 16, 1024), id_s,
-                 kk > 0);
+          const uint32_t off = ((kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32) >> 4;
+          mma_ss_w(tbase + dst, a_desc + off, b_desc + off, id_s, kk > 0);
         }
       };
       bool ok = warp_wait(kv_full, 0, abort_flag, a.err) && warp_wait(&q_full[0], 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
-        mm_s(C::R0, k_addr, q_addr);
+        mm_s(C::R0, k16, d16(q_addr));
         mma_commit_w(s_full);
-        mm_s(C::R1, v_addr, o_addr);
+        mm_s(C::R1, v16, d16(o_addr));
         mma_commit_w(dp_full);
         bool fresh = true;  // next dV / dK start a new tensor-memory sum
         for (int i = 0; i < n; ++i) {
           const int s = i % C::NS;
-          const uint32_t qs = q_addr + s * C::TILE_BYTES, os = o_addr + s * C::TILE_BYTES;
+          const uint64_t qmn = dmn(q_addr + s * C::TILE_BYTES), omn = dmn(o_addr + s * C::TILE_BYTES);
           if (!warp_wait(p_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           // dV += P^T dO: A = P^T (TMEM: each group's bf16 pairs in the first
@@ -326,22 +332,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int kk = 0; kk < kTile / 16; ++kk)
             mma_ts_w(tbase + C::RV,
                    tbase + C::R0 + (kk * 16 / C::GW) * C::GW + ((kk * 16 % C::GW) / 32) * 16 + (kk & 1) * 8,
-                   sdesc_sw128(os + kk * 2048, C::ATOM_BYTES, 1024), id_dkv, !fresh || kk > 0);
+                   omn + (kk * 2048 >> 4), id_dkv, !fresh || kk > 0);
           if (!warp_wait(ds_full, i & 1, abort_flag, a.err)) break;
           tc_fence_after();
           // dQ = dS K: A = dS (dS^T read MN-major), B = K MN-major; first, so
           // the drain of dQ overlaps the dK product
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_ss_w(tbase + C::R1, sdesc_sw128(ds_addr + kk * 2048, C::ATOM_BYTES, 1024),
-                   sdesc_sw128(k_addr + kk * 2048, C::ATOM_BYTES, 1024), id_dq, kk > 0);
+            mma_ss_w(tbase + C::R1, dsmn + (kk * 2048 >> 4), kmn + (kk * 2048 >> 4), id_dq, kk > 0);
           mma_commit_w(dq_full);
           // dK += dS^T Q: A = dS^T K-major (queries contiguous), B = Q MN-major
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
-            mma_ss_w(tbase + C::RK, sdesc_sw128(ds_addr + off, 16, 1024), sdesc_sw128(qs + kk * 2048, C::ATOM_BYTES, 1024),
-                   id_dkv, !fresh || kk > 0);
+            const uint32_t off = ((kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32) >> 4;
+            mma_ss_w(tbase + C::RK, ds16 + off, qmn + (kk * 2048 >> 4), id_dkv, !fresh || kk > 0);
           }
           mma_commit_w(dk_done);
           fresh = false;
@@ -354,11 +358,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             const int s1 = (i + 1) % C::NS;
             if (!warp_wait(&q_full[s1], ((i + 1) / C::NS) & 1, abort_flag, a.err)) break;
             tc_fence_after();
-            mm_s(C::R0, k_addr, q_addr + s1 * C::TILE_BYTES);  // R0's P^T was read by dV(i), issued earlier
+            mm_s(C::R0, k16, d16(q_addr + s1 * C::TILE_BYTES));  // R0's P^T was read by dV(i), issued earlier
             mma_commit_w(s_full);
             if (!warp_wait(dq_empty, i & 1, abort_flag, a.err)) break;
             tc_fence_after();
-            mm_s(C::R1, v_addr, o_addr + s1 * C::TILE_BYTES);
+            mm_s(C::R1, v16, d16(o_addr + s1 * C::TILE_BYTES));
             mma_commit_w(dp_full);
             if (flush) {
               if (!warp_wait(acc_empty, ((i + 1) / kFlush - 1) & 1, abort_flag, a.err)) break;

@@ -237,21 +237,23 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_f16(128, D, false, true);  // P and V in fp16
       const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      // Descriptors built once per tile: an operand's descriptor at byte offset
+      // `off` is its base descriptor plus off / 16 (the 14-bit address field
+      // cannot carry: every shared-memory address is below 256 KB).
       auto qk = [&](int h, int s, int buf) {
+        const uint64_t qa = sdesc_sw128(q_addr + h * C::TILE_BYTES, 16, 1024);
+        const uint64_t kb = sdesc_sw128(k_addr + s * C::TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32;
-          const uint64_t da = sdesc_sw128(q_addr + h * C::TILE_BYTES + off, 16, 1024);
-          const uint64_t db = sdesc_sw128(k_addr + s * C::TILE_BYTES + off, 16, 1024);
-          mma_ss_w(tbase + C::S_COL(buf), da, db, id_qk, kk > 0);
+          const uint32_t off = ((kk >> 2) * C::ATOM_BYTES + (kk & 3) * 32) >> 4;
+          mma_ss_w(tbase + C::S_COL(buf), qa + off, kb + off, id_qk, kk > 0);
         }
       };
       auto pv = [&](int h, int s, int buf, bool acc) {
+        const uint64_t vb = sdesc_sw128(v_addr + s * C::TILE_BYTES, C::ATOM_BYTES, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t db = sdesc_sw128(v_addr + s * C::TILE_BYTES + kk * 2048, C::ATOM_BYTES, 1024);
-          mma_ts_w(tbase + C::O_COL(h), tbase + C::S_COL(buf) + kk * 8, db, id_pv, acc || kk > 0);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          mma_ts_w(tbase + C::O_COL(h), tbase + C::S_COL(buf) + kk * 8, vb + (kk * 2048 >> 4), id_pv, acc || kk > 0);
       };
       // Q K^T of job J = 2 jt + h into buffer J mod NSB; K(jt) is released
       // after its second head
