@@ -740,6 +740,30 @@ def pinned_buffers(w, path, x):
     return host_in, host_out
 
 
+def huge_page_share(tensors):
+    """Share of the bytes of the mappings that hold `tensors` (host buffers from
+    loong_host_alloc, one mapping each) backed by transparent huge pages, from
+    /proc/self/smaps; None where that file cannot be read."""
+    try:
+        lines = open("/proc/self/smaps").read().splitlines()
+    except OSError:
+        return None
+    vmas, cur = {}, None
+    for line in lines:
+        head = line.split(" ", 1)[0]
+        if "-" in head and ":" not in head:
+            lo, hi = head.split("-")
+            cur = int(lo, 16)
+            vmas[cur] = [int(hi, 16) - cur, 0]
+        elif line.startswith("AnonHugePages:") and cur is not None:
+            vmas[cur][1] = int(line.split()[1]) * 1024
+    size = huge = 0
+    for t in tensors:
+        s, h = vmas.get(t.data_ptr(), (0, 0))
+        size, huge = size + s, huge + h
+    return round(huge / size, 4) if size else None
+
+
 def e2e_outputs_match(path, host_out, step, dev):
     """The last end-to-end step's results, read back to the host, against a
     device-only pass over the same inputs: O, LSE, dK, dV bit for bit (their
@@ -828,7 +852,9 @@ def run_e2e(args, w, path, dev, stream, world, pg, x, bufs):
             "api": "loong_attn_2d_host (C ABI, host buffers from loong_host_alloc)",
             "copies": ("library copy streams overlapped with the kernels, two input slots" if overlap
                        else "in series: each call synchronised before the next"),
-            "copy_alone_ms": copy_ms}
+            "copy_alone_ms": copy_ms,
+            "host_huge_page_share": {"in": huge_page_share(host_in.values()),
+                                     "out": huge_page_share(host_out.values())}}
 
 
 def main(argv=None):

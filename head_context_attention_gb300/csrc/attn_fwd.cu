@@ -18,13 +18,17 @@
 // steps) is the online-softmax update itself: O and l carry the reference
 // maximum m, and a step whose maximum exceeds m by more than 2^8 rescales O
 // and l to the new maximum, which is the log-sum-exp merge written in
-// unnormalised form.  In STEPWISE mode the launch covers one ring step and the
-// epilogue merges the step's normalised result into an fp32 accumulator by
-// log-sum-exp.  Non-causal descriptors walk every key tile and mask only the
-// ragged tail of a block.  Q, K, V and O are addressed through a Layout
-// (natural or rank-major, ring.cuh); in STEPWISE_COPY modes K and V are read
-// from the query rank's plane of the receive buffers the exchange filled
-// (exchange.h).  A launch may cover the query rows of a range of ring ranks.
+// unnormalised form.  After a row's first tile the softmax forms P against the
+// running maximum straight away and computes the tile's maximum only when
+// some row of the warp sums to 2^15 or more: a smaller sum bounds every P of
+// the row by 2^15, so no score passed m by more than 2^8.  In STEPWISE mode
+// the launch covers one ring step and the epilogue merges the step's
+// normalised result into an fp32 accumulator by log-sum-exp.  Non-causal
+// descriptors walk every key tile and mask only the ragged tail of a block.
+// Q, K, V and O are addressed through a Layout (natural or rank-major,
+// ring.cuh); in STEPWISE_COPY modes K and V are read from the query rank's
+// plane of the receive buffers the exchange filled (exchange.h).  A launch may
+// cover the query rows of a range of ring ranks.
 //
 // Warp roles (320 threads): warps 0-3 softmax for head slot 0, warps 4-7 for
 // head slot 1 (warp w reads TMEM lanes 32*(w%4)..+31, the rows it owns),
@@ -90,6 +94,10 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // P is formed as exp2(x + kPBias): with the lazy rescale every probability is at
 // most 2^8 relative to the running maximum, so fp16 P stays below 2^15.
 constexpr float kPBias = 7.0f;
+// A tile's row sum of P below this bounds each of its P by the same value:
+// 2^(bias + threshold), the largest P the lazy rescale lets through.
+constexpr float kSumBound = 32768.0f;
+static_assert(kSumBound == float(1 << int(kPBias + kRescaleThreshold)), "sum bound = 2^(bias + threshold)");
 
 template <int D, bool STEP>
 __global__ void __launch_bounds__(320, 1)
@@ -319,75 +327,95 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_after();
       uint32_t sr[4][32];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tmem_ld32(tS + cb * 32, sr[cb]);
-      tmem_wait_ld();
       const int klen = walk.klen();
       const bool dg = walk.diag();
-      if (dg || klen < kTile) {
-        const int lim = dg ? min(row, klen - 1) : klen - 1;
+      // the tile's scores, masked columns at -inf (read again by the full path)
+      auto load_s = [&]() {
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) tmem_ld32(tS + cb * 32, sr[cb]);
+        tmem_wait_ld();
+        if (dg || klen < kTile) {
+          const int lim = dg ? min(row, klen - 1) : klen - 1;
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (cb * 32 + i > lim) sr[cb][i] = __float_as_uint(-INFINITY);
+        }
+      };
+      load_s();
+      // P = exp2(s*scale*log2e - ref + bias) for the whole tile, with the
+      // columns in pairs on the paired fp32 pipe; returns this row's sum of P
+      // (l carries the factor 2^bias as well)
+      uint32_t pk[2][32];
+      auto form_p = [&](float ref) {
+        const float2 sl2v = make_float2(sl2, sl2), nref = make_float2(kPBias - ref, kPBias - ref);
+        float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (cb * 32 + i > lim) sr[cb][i] = __float_as_uint(-INFINITY);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1])),
+                                        sl2v, nref);
+            const float p0 = fast_exp2(x.x);
+            const float p1 = fast_exp2(x.y);
+            lsum = __fadd2_rn(lsum, make_float2(p0, p1));
+            pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_f16(p0, p1);
+          }
+        return lsum.x + lsum.y;
+      };
+      // After the first tile, P is first formed against the running maximum.
+      // A row sum below 2^(bias + threshold) bounds every P of the row by the
+      // same value, so no column passed the running maximum by more than the
+      // threshold: nothing to rescale, and the row maximum is not needed.
+      // Otherwise (or on NaN) the warp takes the full path below.
+      bool full = j == 0;
+      if (!full) {
+        const float ts = form_p(m_run);
+        full = __any_sync(0xffffffffu, !(ts < kSumBound));
+        if (!full) l_run += ts;
       }
-      // row maximum, two new columns per (three-input) max
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (full) {
+        if (j > 0) load_s();  // P of this tile is not stored yet: the scores are still in place
+        // row maximum, two new columns per (three-input) max
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb)
+        for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          mx0 = fmax3(mx0, __uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1]));
-          mx1 = fmax3(mx1, __uint_as_float(sr[cb][i + 2]), __uint_as_float(sr[cb][i + 3]));
-        }
-      const float m_tile = fmaxf(mx0, mx1) * sl2;
-      const float m_new = fmaxf(m_run, m_tile);
-      const bool rescale = j > 0 && m_new > m_run + kRescaleThreshold;
-      if (j == 0) m_run = m_new;
-      // The decision is per row, but TMEM loads and stores are warp-collective:
-      // the whole warp takes the branch, rows that need none scale by 1.
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O_h must hold the previous tile's P V: with two buffers the commit
-        // that signalled these scores follows it; with three, wait for it
-        // (completion j - 1 of pv_done[h]; completion j needs this tile's P)
-        if (C::NSB > 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[h], (j - 1) & 1, abort_flag, a.err))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float f = rescale ? fast_exp2(m_run - m_new) : 1.f;
-        l_run *= f;
+          for (int i = 0; i < 32; i += 4) {
+            mx0 = fmax3(mx0, __uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1]));
+            mx1 = fmax3(mx1, __uint_as_float(sr[cb][i + 2]), __uint_as_float(sr[cb][i + 3]));
+          }
+        const float m_tile = fmaxf(mx0, mx1) * sl2;
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool rescale = j > 0 && m_new > m_run + kRescaleThreshold;
+        if (j == 0) m_run = m_new;
+        // The decision is per row, but TMEM loads and stores are warp-collective:
+        // the whole warp takes the branch, rows that need none scale by 1.
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_h must hold the previous tile's P V: with two buffers the commit
+          // that signalled these scores follows it; with three, wait for it
+          // (completion j - 1 of pv_done[h]; completion j needs this tile's P)
+          if (C::NSB > 2 && !__all_sync(0xffffffffu, mbar_wait(&pv_done[h], (j - 1) & 1, abort_flag, a.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = rescale ? fast_exp2(m_run - m_new) : 1.f;
+          l_run *= f;
 #pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t orow[32];
-          tmem_ld32(tO + cb * 32, orow);
-          tmem_wait_ld();
+          for (int cb = 0; cb < D / 32; ++cb) {
+            uint32_t orow[32];
+            tmem_ld32(tO + cb * 32, orow);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
-          tmem_st32(tO + cb * 32, orow);
+            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * f);
+            tmem_st32(tO + cb * 32, orow);
+          }
+          if (rescale) m_run = m_new;
         }
-        if (rescale) m_run = m_new;
+        l_run += form_p(m_run == -INFINITY ? 0.f : m_run);
       }
-      const float ref = m_run == -INFINITY ? 0.f : m_run;
-      // column pairs on the paired fp32 pipe: x = s*scale*log2e - m + bias, and
-      // the two running sums (each half rounds as the scalar operation would);
-      // l carries the factor 2^bias as well
-      const float2 sl2v = make_float2(sl2, sl2), nref = make_float2(kPBias - ref, kPBias - ref);
-      float2 lsum = make_float2(0.f, 0.f);
-      uint32_t pk[2][32];
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[cb][i]), __uint_as_float(sr[cb][i + 1])),
-                                      sl2v, nref);
-          const float p0 = fast_exp2(x.x);
-          const float p1 = fast_exp2(x.y);
-          lsum = __fadd2_rn(lsum, make_float2(p0, p1));
-          pk[cb >> 1][(cb & 1) * 16 + (i >> 1)] = pack_f16(p0, p1);
-        }
-      l_run += lsum.x + lsum.y;
       tmem_st32(tS, pk[0]);
       tmem_st32(tS + 32, pk[1]);
       tmem_wait_st();

@@ -12,9 +12,11 @@
 // 8192 times fewer pages to translate.
 //
 // A buffer is an anonymous mapping aligned to the huge-page size, advised
-// MADV_HUGEPAGE, faulted in one byte per base page and registered with CUDA
-// (cudaHostRegister).  Without transparent huge pages it is still pinned and
-// works as before.
+// MADV_HUGEPAGE, faulted in one byte per base page, collapsed into huge pages
+// where the fault path fell back to base pages (MADV_COLLAPSE, which compacts
+// memory for this range only; ignored by kernels without it) and registered
+// with CUDA (cudaHostRegister).  Without transparent huge pages it is still
+// pinned and works as before.
 #include <sys/mman.h>
 #include <unistd.h>
 
@@ -25,6 +27,10 @@
 #include <mutex>
 
 #include "internal.h"
+
+#ifndef MADV_COLLAPSE
+#define MADV_COLLAPSE 25  // Linux 6.1 and later
+#endif
 
 namespace loong {
 
@@ -74,6 +80,7 @@ int loong_host_alloc(size_t bytes, void** ptr) {
   char* p = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(raw) + align - 1) / align * align);
   madvise(p, len, MADV_HUGEPAGE);  // advisory: without huge pages the buffer still works
   for (size_t off = 0; off < len; off += page) p[off] = 0;
+  if (align > page) madvise(p, len, MADV_COLLAPSE);  // advisory, as above
   const cudaError_t e = cudaHostRegister(p, len, cudaHostRegisterDefault);
   if (e != cudaSuccess) {
     munmap(raw, raw_bytes);

@@ -119,3 +119,22 @@ def test_kernel_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench.kernel_source_hash() == h0
     (src / bench.KERNEL_SOURCES[0]).write_text("int a = 3;\nint b = 2;\n")
     assert bench.kernel_source_hash() != h0
+
+
+def test_huge_page_share_reads_the_buffer_mappings():
+    """The e2e record's huge-page share: a fraction for buffers that start a
+    mapping (as loong_host_alloc's do), None for memory that does not."""
+    import mmap
+
+    import torch
+
+    if not os.path.exists("/proc/self/smaps"):
+        pytest.skip("no /proc/self/smaps")
+    m = mmap.mmap(-1, 4 << 20)
+    t = torch.frombuffer(m, dtype=torch.uint8)
+    t.fill_(1)
+    share = bench.huge_page_share([t])
+    assert share is not None and 0.0 <= share <= 1.0
+    assert bench.huge_page_share([torch.empty(16)[8:]]) is None
+    del t
+    m.close()
