@@ -71,6 +71,35 @@ def test_forward_with_peaky_keys_matches_oracle(cuda_device, d, mode):
     assert_close("LSE", to64(lse), want_lse, LSE_ATOL, 0.0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_forward_with_stepped_key_levels_matches_oracle(cuda_device, d):
+    """Every 128-key tile gets its own score level, 0 to 40 in log2 units (key
+    feature 0 times query feature 0, the rest small noise), in a seeded order.
+    Along a walk the running maximum then meets tiles a few units above it
+    (P sums past 2^15 with no rescale: the softmax falls back to the full
+    path and keeps its maximum), tiles more than 8 units above it (a rescale)
+    and tiles far below it.  Query rows weight the level by 1, 1/2 or 0, so
+    one warp mixes rows of each kind."""
+    w = inputs.Workload("stepped-levels", 4096, 4, 2, d, 2, 4, 2, 2, False, placement=1)
+    x = inputs.make_inputs(w, device="cuda", with_do=False)
+    g = torch.Generator().manual_seed(20260)
+    ntile = w.seqlen // 128
+    level = torch.randint(0, 21, (ntile,), generator=g).double() * 2.0          # log2 units
+    a = (level * (d ** 0.5) / np.log2(np.e)).repeat_interleave(128)              # s = a / sqrt(d) in nats
+    k = torch.randn(w.batch, w.seqlen, w.hkv, d, generator=g) * 0.05
+    k[..., 0] = a.float()[None, :, None]
+    q = torch.randn(w.batch, w.seqlen, w.hq, d, generator=g) * 0.05
+    wq = torch.tensor([1.0, 0.5, 1.0, 0.0]).repeat(w.seqlen // 4)
+    q[..., 0] = wq[None, :, None]
+    x["q"] = q.to(torch.bfloat16).cuda()
+    x["k"] = k.to(torch.bfloat16).cuda()
+    o, lse, _ = ops.attn_fwd(w, x["q"], x["k"], x["v"])
+    assert ops.loong_get_device_status() == ops.LOONG_OK
+    want_o, want_lse = _oracle(w, x)
+    assert_close("O", to64(o), want_o, O_ATOL, O_RTOL)
+    assert_close("LSE", to64(lse), want_lse, LSE_ATOL, 0.0)
+
+
 def test_chunked_oracle_agrees_on_gpu_inputs(cuda_device):
     """The GPU result also matches the second (ring-walking) oracle."""
     w = _workload("d128-double-ring")
