@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   QWalk walk;
   walk.init(g, a.G, bk, kt, a.t_begin, a.t_end);
-  const int n = walk.count();
+  const int n = walk.total();
   if (n == 0) return;
   const int nflush = (n - 1) / kFlush;  // flushes before the final write
 

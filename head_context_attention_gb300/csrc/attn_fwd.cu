@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(320, 1)
 
   KvWalk walk;
   walk.init(g, bq, qi, a.t_begin, a.t_end);
-  const int n = walk.count();
+  const int n = walk.total();
   if (n == 0) return;  // uniform over the CTA: nothing of this tile in these steps
 
   const int warp = threadIdx.x >> 5;

@@ -116,12 +116,14 @@ struct Layout {
 struct KvWalk {
   RingGeom g;
   int c, bq, qi, t, t1, part, kt, kt_n, bk;
+  int t_first;  // the first step of the walk
 
   __host__ __device__ void init(const RingGeom& geom, int bq_, int qi_, int t0, int t1_) {
     g = geom;
     bq = bq_;
     qi = qi_;
     c = block_owner(g, bq);
+    t_first = t0;
     t = t0;
     t1 = t1_;
     part = 0;
@@ -158,6 +160,15 @@ struct KvWalk {
       ++t;
     }
     settle();
+  }
+  // Number of tiles of the whole walk, right after init.  Over every ring
+  // step each block is visited once, so the count has a closed form: every
+  // tile of every earlier block and the diagonal block up to qi (causal), or
+  // every tile (non-causal).  A partial range of steps walks a copy.
+  __host__ __device__ int total() const {
+    if (t_first == 0 && t1 == g.inner * g.outer)
+      return g.causal ? bq * g.ntile + qi + 1 : g.nblocks * g.ntile;
+    return count();
   }
   // Number of tiles left, walking a copy.
   __host__ __device__ int count() const {
@@ -196,6 +207,7 @@ __host__ __device__ inline int ring_dst(int j, int t, int inner, int outer) {
 struct QWalk {
   RingGeom g;
   int G, bk, kt, j, t, t1, part, rot;
+  int t_first;  // the first step of the walk
   int qlo, len, k, hk;  // tiles [qlo, ntile) of the current block; position k; head position hk
   int rot_len, rot_g;   // rot reduced modulo len (per block) and modulo G
   int qi, head, bq;
@@ -206,6 +218,7 @@ struct QWalk {
     bk = bk_;
     kt = kt_;
     j = block_owner(g, bk);
+    t_first = t0;
     t = t0;
     t1 = t1_;
     part = 0;
@@ -264,6 +277,15 @@ struct QWalk {
     return e < kTile ? e : kTile;
   }
   __host__ __device__ bool diag() const { return g.causal && bq == bk && qi == kt; }
+  // Number of (tile, head) pairs of the whole walk, right after init: over
+  // every ring step each query block is visited once (closed form: every
+  // tile of every later block and the key tile's own block from kt on, or
+  // every tile when non-causal), else a copy is walked.
+  __host__ __device__ int total() const {
+    if (t_first == 0 && t1 == g.inner * g.outer)
+      return G * (g.causal ? (g.nblocks - 1 - bk) * g.ntile + g.ntile - kt : g.nblocks * g.ntile);
+    return count();
+  }
   __host__ __device__ int count() const {
     int n = 0;
     for (int tt = t; tt < t1; ++tt) {
