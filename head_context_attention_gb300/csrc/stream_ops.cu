@@ -400,59 +400,63 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const __grid_constan
 }
 
 // Backward row statistics (see stat_row_len): for row (b, s, h) of O and dO
-// (rows enumerated in natural order, read where `lay` keeps them),
-// D = sum_d dO*O in fp32 and LSE*log2(e), written at the padded position of
-// token s.  With o_res, O is taken as O + O_res (exact in fp32: the residual
-// holds the next 8 bits).  16 threads per row of 128 bf16 (8 elements each),
-// 8 for d = 64.
+// (read where `lay` keeps them), D = sum_d dO*O in fp32 and LSE*log2(e),
+// written at the padded position of token s.  With o_res, O is taken as
+// O + O_res (exact in fp32: the residual holds the next 8 bits).  16 threads
+// per row of 128 bf16 (8 elements each), 8 for d = 64.  A block covers
+// consecutive tokens of one head (blockIdx.y) of one sequence (blockIdx.z),
+// so a thread finds its token and part by shifts; only the layout map and
+// the block position divide (32-bit).
 template <int D>
-__global__ void bwd_rowstats_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_res,
-                                    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, float* __restrict__ lse2,
-                                    float* __restrict__ dstat, int64_t rows, int64_t S, int hq, int blk,
-                                    int blk_pad, int64_t stat_len, Layout lay, unsigned* err) {
-  constexpr int TPR = D / 8;
-  const int64_t total = rows * TPR;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+__global__ void __launch_bounds__(256) bwd_rowstats_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ o_res,
+    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse, float* __restrict__ lse2,
+    float* __restrict__ dstat, int64_t rows, int S, int hq, int blk, int blk_pad, int64_t stat_len, Layout lay,
+    unsigned* err) {
+  constexpr int TPR = D / 8;         // threads per row
+  constexpr int RPB = 256 / TPR;     // rows (tokens) per block and pass
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int part = threadIdx.x % TPR;
+  const int lane_row = (threadIdx.x & 31) / TPR;  // this lane's row within its warp
+  const int64_t bh = static_cast<int64_t>(b) * hq + h;
   // The loop runs per warp (lanes leave together) so the shuffles below see
   // every lane; TPR divides 32, so a row's lanes are all live or all idle.
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-       i - static_cast<int64_t>(threadIdx.x & 31) < total; i += stride) {
-    const bool live = i < total;
-    const int64_t row = live ? i / TPR : 0;
-    const int part = static_cast<int>(i % TPR);
-    // row = (b*S + s)*hq + h
-    const int64_t h = row % hq;
-    const int64_t bs = row / hq;
-    const int64_t b = bs / S;
-    const int64_t s = bs - b * S;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * RPB;
+  for (int64_t s = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / TPR; s - lane_row < S; s += step) {
+    const bool live = s < S;
     float acc = 0.f;
-    const int64_t off = lay.vec(static_cast<int>(b), s, static_cast<int>(h), hq) * D;
-    // checked build: the row's O / dO vectors lie inside the tensors
-    const bool row_ok = !live || in_bounds(off >= 0 && off + D <= rows * D, err);
-    if (live && row_ok) {
-      const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + off) + part);
-      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + off) + part);
-      const uint4 rv = o_res ? __ldg(reinterpret_cast<const uint4*>(o_res + off) + part) : make_uint4(0, 0, 0, 0);
-      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
-      const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
+    bool row_ok = true;
+    if (live) {
+      const int64_t off = lay.vec(b, s, h, hq) * D;
+      // checked build: the row's O / dO vectors lie inside the tensors
+      row_ok = in_bounds(off >= 0 && off + D <= rows * D, err);
+      if (row_ok) {
+        const uint4 ov = __ldg(reinterpret_cast<const uint4*>(o + off) + part);
+        const uint4 gv = __ldg(reinterpret_cast<const uint4*>(dout + off) + part);
+        const uint4 rv = o_res ? __ldg(reinterpret_cast<const uint4*>(o_res + off) + part) : make_uint4(0, 0, 0, 0);
+        const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+        const __nv_bfloat162* r2 = reinterpret_cast<const __nv_bfloat162*>(&rv);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 fa = __bfloat1622float2(a2[e]);
-        const float2 fr = __bfloat1622float2(r2[e]);
-        const float2 fb = __bfloat1622float2(b2[e]);
-        acc = fmaf(fa.x + fr.x, fb.x, acc);
-        acc = fmaf(fa.y + fr.y, fb.y, acc);
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = __bfloat1622float2(a2[e]);
+          const float2 fr = __bfloat1622float2(r2[e]);
+          const float2 fb = __bfloat1622float2(b2[e]);
+          acc = fmaf(fa.x + fr.x, fb.x, acc);
+          acc = fmaf(fa.y + fr.y, fb.y, acc);
+        }
       }
     }
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && part == 0) {
-      const int64_t blk_i = s / blk;
-      const int64_t pos = (b * hq + h) * stat_len + blk_i * blk_pad + (s - blk_i * blk);
-      if (row_ok && in_bounds(pos >= 0 && pos < (b * hq + h + 1) * stat_len, err)) {
+    if (live && part == 0 && row_ok) {
+      const int si = static_cast<int>(s);  // s < S < 2^31
+      const int blk_i = si / blk;
+      const int64_t pos = bh * stat_len + static_cast<int64_t>(blk_i) * blk_pad + (si - blk_i * blk);
+      if (in_bounds(pos >= 0 && pos < (bh + 1) * stat_len, err)) {
         dstat[pos] = acc;
-        lse2[pos] = lse[(b * hq + h) * S + s] * kLog2e;
+        lse2[pos] = lse[bh * S + s] * kLog2e;
       }
     }
   }
@@ -582,12 +586,20 @@ int launch_bwd_rowstats(const loong_attn_desc& d, const void* o, const void* o_r
   const int bp = stat_block_pad(g.blk);
   unsigned* err = device_error_word();
   if (!err) return LOONG_ERR_CUDA;
+  // grid: (passes over the tokens, heads, sequences); about 32 blocks of 256
+  // threads per SM in all, each striding over its (head, sequence) slice
+  if (d.hq > 65535 || d.batch > 65535) return LOONG_ERR_INVALID_ARG;
+  const int rpb = 256 / (d.head_dim / 8);
+  const int64_t slices = static_cast<int64_t>(d.hq) * d.batch;
+  const int64_t want = std::max<int64_t>(1, static_cast<int64_t>(num_sms()) * 32 / slices);
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>((d.seqlen + rpb - 1) / rpb, want)),
+                  static_cast<unsigned>(d.hq), static_cast<unsigned>(d.batch));
   if (d.head_dim == 128)
-    bwd_rowstats_kernel<128><<<grid_for(rows * 16, 256, 8), 256, 0, stream>>>(
-        po, pr, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
+    bwd_rowstats_kernel<128><<<grid, 256, 0, stream>>>(po, pr, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk,
+                                                       bp, stat_len, layout_of(d), err);
   else if (d.head_dim == 64)
-    bwd_rowstats_kernel<64><<<grid_for(rows * 8, 256, 8), 256, 0, stream>>>(
-        po, pr, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk, bp, stat_len, layout_of(d), err);
+    bwd_rowstats_kernel<64><<<grid, 256, 0, stream>>>(po, pr, pd, lse, lse2, dstat, rows, d.seqlen, d.hq, g.blk,
+                                                      bp, stat_len, layout_of(d), err);
   else
     return LOONG_ERR_UNSUPPORTED;
   return check_launch();
