@@ -21,7 +21,9 @@
 // unnormalised form.  After a row's first tile the softmax forms P against the
 // running maximum straight away and computes the tile's maximum only when
 // some row of the warp sums to 2^15 or more: a smaller sum bounds every P of
-// the row by 2^15, so no score passed m by more than 2^8.  In STEPWISE mode
+// the row by 2^15, so no score passed m by more than 2^8.  A row whose sum
+// reached the bound then takes the tile's maximum as its reference, so its
+// later tiles pass the test again.  In STEPWISE mode
 // the launch covers one ring step and the epilogue merges the step's
 // normalised result into an fp32 accumulator by log-sum-exp.  Non-causal
 // descriptors walk every key tile and mask only the ragged tail of a block.
@@ -370,9 +372,11 @@ __global__ void __launch_bounds__(320, 1)
       // threshold: nothing to rescale, and the row maximum is not needed.
       // Otherwise (or on NaN) the warp takes the full path below.
       bool full = j == 0;
+      bool over = false;  // this row's sum reached the bound
       if (!full) {
         const float ts = form_p(m_run);
-        full = __any_sync(0xffffffffu, !(ts < kSumBound));
+        over = !(ts < kSumBound);
+        full = __any_sync(0xffffffffu, over);
         if (!full) l_run += ts;
       }
       if (full) {
@@ -388,7 +392,10 @@ __global__ void __launch_bounds__(320, 1)
           }
         const float m_tile = fmaxf(mx0, mx1) * sl2;
         const float m_new = fmaxf(m_run, m_tile);
-        const bool rescale = j > 0 && m_new > m_run + kRescaleThreshold;
+        // A row whose sum reached the bound takes the new maximum even below the
+        // threshold (its maximum is then above the reference): a reference
+        // left low would send the warp down this path on every later tile.
+        const bool rescale = j > 0 && m_new > m_run + (over ? 0.f : kRescaleThreshold);
         if (j == 0) m_run = m_new;
         // The decision is per row, but TMEM loads and stores are warp-collective:
         // the whole warp takes the branch, rows that need none scale by 1.
