@@ -381,7 +381,10 @@ LOONG_API int loong_attn_2d_host(const loong_attn_desc* desc, int32_t slot, cons
  * and when those translations have gone cold (a few seconds without copies,
  * or after kernels that sweep much device memory) each page costs a miss.
  * Measured with 64 KB base pages, a 2.7 GB host-to-device copy then took
- * 360-380 ms from cudaHostAlloc memory and 12.7 ms from huge pages.
+ * 360-380 ms from cudaHostAlloc memory and 12.7 ms from huge pages.  The
+ * range is also asked to collapse into huge pages (MADV_COLLAPSE, where the
+ * kernel has it).  On some hosts device writes into the buffer split part of
+ * it back into base pages, and copies into it slow down again.
  *   bytes == 0 sets *ptr = NULL.  The caller owns the buffer and releases it
  *   with loong_host_free.  Returns LOONG_OK, LOONG_ERR_INVALID_ARG (null
  *   ptr), or LOONG_ERR_CUDA (mapping or registration failed; *ptr = NULL).
